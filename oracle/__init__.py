@@ -1,0 +1,198 @@
+"""CPU oracle for the NVFP4 training quantizer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The product
+path (``tensor_quantization_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``nvfp4_oracle.c`` (plain single-threaded C, fp32 IEEE,
+no FMA contraction); this module compiles it with gcc on first use and wraps it
+with ctypes.  Inputs are numpy arrays: bf16 data is passed as its uint16 bit
+pattern, fp32 as float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_SO = os.path.join(_HERE, "_liboracle.so")
+_LOCK = threading.Lock()
+_LIB = None
+
+MODES = {"rne": 0, "sr": 1, "4o6": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_liboracle.so`` (gcc, no fast math)."""
+    with _LOCK:
+        fresh = os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)
+        if force or not fresh:
+            tmp = _SO + f".{os.getpid()}.tmp"
+            cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                   "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _SO)
+    return _SO
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        lib = ctypes.CDLL(build())
+        i64, i32, u32, u64, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
+        lib.ora_quantize.argtypes = [vp, i32, i64, i64, i64, i32, i32, i32, i32, i32, i32, u32,
+                                     u64, u64, i64, i64, vp, vp, vp, vp]
+        lib.ora_quantize.restype = i32
+        lib.ora_dequantize.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, i32]
+        lib.ora_dequantize.restype = i32
+        lib.ora_amax.argtypes = [vp, i32, i64, i64, i64, i32, i32, u32, i32, vp, vp]
+        lib.ora_amax.restype = i32
+        lib.ora_e2m1_value.argtypes = [i32]
+        lib.ora_e2m1_value.restype = ctypes.c_float
+        lib.ora_e2m1_rne.argtypes = [ctypes.c_float]
+        lib.ora_e2m1_rne.restype = i32
+        lib.ora_e2m1_sr.argtypes = [ctypes.c_float, ctypes.c_uint]
+        lib.ora_e2m1_sr.restype = i32
+        lib.ora_e4m3_value.argtypes = [ctypes.c_uint]
+        lib.ora_e4m3_value.restype = ctypes.c_float
+        lib.ora_e4m3_rn.argtypes = [ctypes.c_float]
+        lib.ora_e4m3_rn.restype = ctypes.c_uint
+        lib.ora_philox4x32_10.argtypes = [vp, vp, vp]
+        lib.ora_philox4x32_10.restype = None
+        lib.ora_rht16.argtypes = [vp, u32]
+        lib.ora_rht16.restype = None
+        lib.ora_swizzle_offset.argtypes = [i64, i64, i64]
+        lib.ora_swizzle_offset.restype = i64
+        lib.ora_scale_bytes.argtypes = [i64, i64, i32]
+        lib.ora_scale_bytes.restype = i64
+        lib.ora_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.ora_f32_to_bf16.restype = ctypes.c_uint16
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _input(x: np.ndarray):
+    if x.ndim != 2:
+        raise ValueError("oracle input must be 2-D")
+    if x.dtype == np.uint16:
+        dtype = 0
+    elif x.dtype == np.float32:
+        dtype = 1
+    else:
+        raise ValueError("oracle input must be uint16 (bf16 bits) or float32")
+    if x.strides[1] != x.itemsize or x.strides[0] % x.itemsize:
+        x = np.ascontiguousarray(x)
+    ld = x.strides[0] // x.itemsize if x.shape[0] > 1 else x.shape[1]
+    return x, dtype, ld
+
+
+def scale_bytes(rows_out: int, cols_out: int, swizzled: bool) -> int:
+    return int(_lib().ora_scale_bytes(rows_out, cols_out, int(swizzled)))
+
+
+def quantize(x: np.ndarray, *, colwise: bool = False, mode: str = "rne", block2d: bool = False,
+             per_row: bool = False, swizzled: bool = False, rht: bool = False, sign_mask: int = 0,
+             seed: int = 0, offset: int = 0, row_range: tuple[int, int] | None = None) -> dict:
+    """Quantize one orientation of ``x``; returns codes, scales, amax, global_scale.
+
+    ``colwise`` works on X^T.  ``row_range`` restricts encoding to output rows
+    [r0, r1) (the per-tensor amax still covers the whole tensor); rows outside
+    the range are left zero.
+    """
+    x, dtype, ld = _input(x)
+    rows, cols = x.shape
+    R, C = (cols, rows) if colwise else (rows, cols)
+    r0, r1 = row_range if row_range is not None else (0, R)
+    codes = np.zeros((R, C // 2), np.uint8)
+    scales = np.zeros(scale_bytes(R, C, swizzled), np.uint8)
+    n_g = R if per_row else 1
+    amax = np.zeros(n_g, np.float32)
+    gs = np.zeros(n_g, np.float32)
+    rc = _lib().ora_quantize(_ptr(x), dtype, rows, cols, ld, int(colwise), MODES[mode], int(block2d),
+                             int(per_row), int(swizzled), int(rht), sign_mask & 0xFFFF, seed, offset,
+                             r0, r1, _ptr(codes), _ptr(scales), _ptr(amax), _ptr(gs))
+    if rc != 0:
+        raise ValueError(f"oracle quantize rejected the arguments (status {rc})")
+    if not swizzled:
+        scales = scales.reshape(R, C // 16)
+    return {"codes": codes, "scales": scales, "amax": amax, "global_scale": gs}
+
+
+def dequantize(codes: np.ndarray, scales: np.ndarray, global_scale: np.ndarray, rows: int, cols: int,
+               *, swizzled: bool = False, per_row: bool = False, out_dtype: str = "fp32") -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    gsc = np.ascontiguousarray(global_scale, np.float32)
+    out = np.zeros((rows, cols), np.uint16 if out_dtype == "bf16" else np.float32)
+    rc = _lib().ora_dequantize(_ptr(codes), _ptr(scales), _ptr(gsc), rows, cols, int(swizzled),
+                               int(per_row), _ptr(out), 0 if out_dtype == "bf16" else 1)
+    if rc != 0:
+        raise ValueError(f"oracle dequantize rejected the arguments (status {rc})")
+    return out
+
+
+def amax(x: np.ndarray, *, colwise: bool = False, rht: bool = False, sign_mask: int = 0,
+         per_row: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    x, dtype, ld = _input(x)
+    rows, cols = x.shape
+    R = cols if colwise else rows
+    n = R if per_row else 1
+    a = np.zeros(n, np.float32)
+    g = np.zeros(n, np.float32)
+    rc = _lib().ora_amax(_ptr(x), dtype, rows, cols, ld, int(colwise), int(rht), sign_mask & 0xFFFF,
+                         int(per_row), _ptr(a), _ptr(g))
+    if rc != 0:
+        raise ValueError(f"oracle amax rejected the arguments (status {rc})")
+    return a, g
+
+
+# ---- scalar building blocks (exposed for the pin tests) ----
+def e2m1_value(code: int) -> float:
+    return float(_lib().ora_e2m1_value(code))
+
+
+def e2m1_rne(q: float) -> int:
+    return int(_lib().ora_e2m1_rne(q))
+
+
+def e2m1_sr(q: float, r: int) -> int:
+    return int(_lib().ora_e2m1_sr(q, r))
+
+
+def e4m3_value(b: int) -> float:
+    return float(_lib().ora_e4m3_value(b))
+
+
+def e4m3_rn(s: float) -> int:
+    return int(_lib().ora_e4m3_rn(s))
+
+
+def philox4x32_10(ctr, key) -> list[int]:
+    c = np.array(ctr, np.uint32)
+    k = np.array(key, np.uint32)
+    o = np.zeros(4, np.uint32)
+    _lib().ora_philox4x32_10(_ptr(c), _ptr(k), _ptr(o))
+    return [int(v) for v in o]
+
+
+def rht16(v, sign_mask: int) -> np.ndarray:
+    a = np.array(v, np.float32).copy()
+    _lib().ora_rht16(_ptr(a), sign_mask & 0xFFFF)
+    return a
+
+
+def swizzle_offset(r: int, j: int, cs_padded: int) -> int:
+    return int(_lib().ora_swizzle_offset(r, j, cs_padded))
+
+
+def f32_to_bf16(f: float) -> int:
+    return int(_lib().ora_f32_to_bf16(f))
