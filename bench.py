@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Throughput of the NVFP4 quantizer's hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole path over one batch: the global amax pass and
+the fused quantize (RHT + Philox stochastic rounding + E4M3/E2M1 encode +
+packing + 32x4x4-swizzled scales) over an 8192x4096 bf16 activation with 0.1%
+outlier columns.  The metric is effective HBM GB/s: bf16 bytes read (the amax
+pass included) plus codes, scales and the scale words written, divided by the
+step time.  Inputs are resident in HBM before the timed region and the L2 is
+flushed (512 MiB write) before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores (the pages publish no runnable implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tensor_quantization_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "NVFP4 quantize effective HBM GB/s and % of GB300 peak (8192×4096 bf16, RHT+SR)"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- bytes
+def scale_bytes(rows_out: int, cols_out: int, swizzled: bool) -> int:
+    cs = cols_out // 16
+    if not swizzled:
+        return rows_out * cs
+    return ((rows_out + 127) // 128 * 128) * ((cs + 3) // 4 * 4)
+
+
+def orientations(w: wl.Workload):
+    out = []
+    if w.rowwise:
+        out.append((w.rows, w.cols))
+    if w.colwise:
+        out.append((w.cols, w.rows))
+    return out
+
+
+def counted_bytes(w: wl.Workload, elem: int = 2) -> dict:
+    """Algorithmic bytes of one step.  Per tensor: the amax pass reads the input
+    and writes amax and g (8 B); the encode reads it again and writes codes and
+    scales.  Per row: one read serves both, plus 8 B of scale words per row."""
+    n = w.rows * w.cols
+    codes = sum(r * c // 2 for r, c in orientations(w))
+    scales = sum(scale_bytes(r, c, w.swizzled) for r, c in orientations(w))
+    if w.per_row:
+        q = n * elem + codes + scales + 8 * w.rows
+        return {"amax_pass": 0, "quantize": q, "total": q}
+    a, q = n * elem + 8, n * elem + codes + scales
+    return {"amax_pass": a, "quantize": q, "total": a + q}
+
+
+# ---------------------------------------------------------------- peaks
+def hbm_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if its recorded source digest matches the current sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_quantization_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read only) on a
+    background thread while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period, self._stop = period_s, threading.Event()
+        self.ok = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.nv, self.h, self.ok = nv, h, True
+        except OSError:
+            pass
+
+    def _run(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self) -> dict:
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml" if self.ok else "unavailable"}
+
+
+# ----------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int) -> dict | None:
+    from tensor_quantization_gb300 import build, nvfp4
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    nvfp4.load()
+    w = wl.WORKLOADS[args.workload]
+    x_cpu, mask = wl.make_input(w)
+    x = x_cpu.to(dev)
+    R, C = w.rows, w.cols
+    flags = (nvfp4.ROWWISE if w.rowwise else 0) | (nvfp4.COLWISE if w.colwise else 0) | \
+        (nvfp4.SWIZZLED if w.swizzled else 0) | (nvfp4.BLOCK_2D if w.block2d else 0) | \
+        (nvfp4.SCALE_PER_ROW if w.per_row else 0)
+    q = nvfp4.alloc_outputs(x, flags)
+    out = nvfp4.make_output(q.codes_row, q.scales_row, q.codes_col, q.scales_col, q.amax, q.global_scale)
+    ws = nvfp4.Workspace.get(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    split = not w.per_row  # per-tensor: amax pass then encode, timed separately
+
+    def quant_call(fl):
+        if w.mode == "sr" and w.rht:
+            nvfp4.nvfp4_quantize_rht_sr(x, fl, mask, w.philox_seed, w.philox_offset, out, ws, stream)
+        elif w.mode == "sr":
+            nvfp4.nvfp4_quantize_sr(x, fl, w.philox_seed, w.philox_offset, out, ws, stream)
+        elif w.mode == "4o6":
+            nvfp4.nvfp4_quantize_four_over_six(x, fl, out, ws, stream)
+        else:
+            nvfp4.nvfp4_quantize_rne(x, fl, out, ws, stream)
+
+    orient_flag = nvfp4.COLWISE if (w.colwise and not w.rowwise) else nvfp4.ROWWISE
+
+    def step(ev0, ev1, ev2):
+        ev0.record(stream)
+        if split:
+            nvfp4.nvfp4_amax(x, orient_flag, w.rht, mask, out, ws, stream)
+            ev1.record(stream)
+            quant_call(flags | nvfp4.AMAX_GIVEN)
+        else:
+            ev1.record(stream)
+            quant_call(flags)
+        ev2.record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(*[torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            step(*evs[k])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the public API: pinned host input -> device, the
+    # fused call (amax pass + encode), codes/scales/scale words -> pinned host
+    x_host = x_cpu.pin_memory()
+    host_out = {k: torch.empty(getattr(q, k).shape, dtype=getattr(q, k).dtype, pin_memory=True)
+                for k in ("codes_row", "scales_row", "codes_col", "scales_col", "amax", "global_scale")
+                if getattr(q, k) is not None}
+    e2e_ms = []
+    for k in range(max(3, min(args.steps, 20)) + 2):
+        flush.fill_(7)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.copy_(x_host, non_blocking=True)
+        quant_call(flags)
+        for name, h in host_out.items():
+            h.copy_(getattr(q, name), non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        if k >= 2:
+            e2e_ms.append(a.elapsed_time(b))
+    h2d = x_cpu.numel() * x_cpu.element_size()
+    d2h = sum(h.numel() * h.element_size() for h in host_out.values())
+
+    nbytes = counted_bytes(w)
+    ms = total_ms / args.steps
+    value = world * nbytes["total"] / (ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    k1, k2 = statistics.mean(k1_ms), statistics.mean(k2_ms)
+    if split and k1 > k2:
+        dom, dom_bytes, dom_ms, unit_desc = "k_amax", nbytes["amax_pass"], k1, "2 B read per element"
+    else:
+        dom, dom_bytes, dom_ms = "k_quant", nbytes["quantize"], k2
+        unit_desc = "2 B read + 0.5 B codes + 1/16 B scale per element (+ scale words)"
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = profile_traffic(dom, w.name)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "rows": R, "cols": C, "input": "bf16", "mode": w.mode, "rht": w.rht,
+                   "scales": "swizzled_32x4x4" if w.swizzled else "linear",
+                   "l2": "flushed by a 512 MiB write before every timed step",
+                   "parallelism": f"replicas{world}" if world > 1 else "single_gpu"},
+        "counted_bytes_per_step": nbytes["total"],
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": dom_bytes,
+                     "per_unit": unit_desc, "ms_per_launch": round(dom_ms, 5)},
+        "kernels_ms": {"k_amax": round(k1, 5) if split else None, "k_quant": round(k2, 5)},
+        "e2e": {"value": round(nbytes["total"] / (statistics.mean(e2e_ms) * 1e-3) / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(statistics.mean(e2e_ms), 4)},
+        "gpu_launches": args.steps * (2 if split else 1) + (args.steps if pad_launch_needed(w) else 0),
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 4),
+    }
+    return res
+
+
+def pad_launch_needed(w: wl.Workload) -> bool:
+    if not w.swizzled:
+        return False
+    for r, c in orientations(w):
+        if r % 128 or (c // 16) % 4:
+            return True
+    return False
+
+
+# ------------------------------------------------------------ the oracle
+def oracle_sample(w: wl.Workload, x_cpu: torch.Tensor, mask: int, rows: int):
+    """One oracle pass (amax + encode) over the first `rows` rows."""
+    import numpy as np
+
+    import oracle
+    xs = x_cpu[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    for colwise in ([False] if w.rowwise else []) + ([True] if w.colwise else []):
+        oracle.quantize(xs, colwise=colwise, mode=w.mode, block2d=w.block2d, per_row=w.per_row,
+                        swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset)
+
+
+def cpu_baseline(w: wl.Workload, x_cpu: torch.Tensor, mask: int, min_seconds: float) -> dict:
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_sample(w, x_cpu, mask, w.rows)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    gbs = reps * counted_bytes(w)["total"] / el / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full pass(es) of the {w.rows}x{w.cols} workload, single-threaded C oracle, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args) -> dict:
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    x_cpu, mask = wl.make_input(w)
+    rows = 1024 if w.rows >= 1024 else w.rows
+    sub = wl.Workload(**{**w.__dict__, "rows": rows})
+    for _ in range(args.warmup):
+        oracle_sample(w, x_cpu, mask, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample(w, x_cpu, mask, rows)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    v = counted_bytes(sub)["total"] / (ms * 1e-3) / 1e9
+    sample = f"rows 0..{rows} of the {w.rows}x{w.cols} workload per step (amax + encode), single-threaded C oracle"
+    return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "input": "bf16", "mode": w.mode,
+                       "rht": w.rht, "sample_rows": rows},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.HEADLINE, choices=list(wl.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (0 = skip)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if args.cpu_seconds > 0:
+            w = wl.WORKLOADS[args.workload]
+            x_cpu, mask = wl.make_input(w)
+            res["cpu_baseline"] = cpu_baseline(w, x_cpu, mask, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -46,7 +46,7 @@ def _lib():
         lib = ctypes.CDLL(build())
         i64, i32, u32, u64, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
         lib.ora_quantize.argtypes = [vp, i32, i64, i64, i64, i32, i32, i32, i32, i32, i32, u32,
-                                     u64, u64, i64, i64, vp, vp, vp, vp]
+                                     u64, u64, i64, i64, vp, vp, vp, vp, vp]
         lib.ora_quantize.restype = i32
         lib.ora_dequantize.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, i32]
         lib.ora_dequantize.restype = i32
@@ -70,6 +70,12 @@ def _lib():
         lib.ora_swizzle_offset.restype = i64
         lib.ora_scale_bytes.argtypes = [i64, i64, i32]
         lib.ora_scale_bytes.restype = i64
+        lib.ora_e2m1_rne_n.argtypes = [vp, i64, vp]
+        lib.ora_e2m1_rne_n.restype = None
+        lib.ora_e2m1_sr_n.argtypes = [vp, vp, i64, vp]
+        lib.ora_e2m1_sr_n.restype = None
+        lib.ora_e4m3_rn_n.argtypes = [vp, i64, vp]
+        lib.ora_e4m3_rn_n.restype = None
         lib.ora_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.ora_f32_to_bf16.restype = ctypes.c_uint16
         _LIB = lib
@@ -101,12 +107,13 @@ def scale_bytes(rows_out: int, cols_out: int, swizzled: bool) -> int:
 
 def quantize(x: np.ndarray, *, colwise: bool = False, mode: str = "rne", block2d: bool = False,
              per_row: bool = False, swizzled: bool = False, rht: bool = False, sign_mask: int = 0,
-             seed: int = 0, offset: int = 0, row_range: tuple[int, int] | None = None) -> dict:
+             seed: int = 0, offset: int = 0, row_range: tuple[int, int] | None = None,
+             amax_given: float | None = None) -> dict:
     """Quantize one orientation of ``x``; returns codes, scales, amax, global_scale.
 
     ``colwise`` works on X^T.  ``row_range`` restricts encoding to output rows
     [r0, r1) (the per-tensor amax still covers the whole tensor); rows outside
-    the range are left zero.
+    the range are left zero.  ``amax_given`` replaces the per-tensor amax.
     """
     x, dtype, ld = _input(x)
     rows, cols = x.shape
@@ -117,9 +124,11 @@ def quantize(x: np.ndarray, *, colwise: bool = False, mode: str = "rne", block2d
     n_g = R if per_row else 1
     amax = np.zeros(n_g, np.float32)
     gs = np.zeros(n_g, np.float32)
+    given = None if amax_given is None else np.array([amax_given], np.float32)
     rc = _lib().ora_quantize(_ptr(x), dtype, rows, cols, ld, int(colwise), MODES[mode], int(block2d),
                              int(per_row), int(swizzled), int(rht), sign_mask & 0xFFFF, seed, offset,
-                             r0, r1, _ptr(codes), _ptr(scales), _ptr(amax), _ptr(gs))
+                             r0, r1, None if given is None else _ptr(given),
+                             _ptr(codes), _ptr(scales), _ptr(amax), _ptr(gs))
     if rc != 0:
         raise ValueError(f"oracle quantize rejected the arguments (status {rc})")
     if not swizzled:
@@ -196,3 +205,25 @@ def swizzle_offset(r: int, j: int, cs_padded: int) -> int:
 
 def f32_to_bf16(f: float) -> int:
     return int(_lib().ora_f32_to_bf16(f))
+
+
+def e2m1_rne_array(q: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, np.float32)
+    out = np.zeros(q.size, np.uint8)
+    _lib().ora_e2m1_rne_n(_ptr(q), q.size, _ptr(out))
+    return out
+
+
+def e2m1_sr_array(q: np.ndarray, r: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, np.float32)
+    r = np.ascontiguousarray(r, np.uint8)
+    out = np.zeros(q.size, np.uint8)
+    _lib().ora_e2m1_sr_n(_ptr(q), _ptr(r), q.size, _ptr(out))
+    return out
+
+
+def e4m3_rn_array(s: np.ndarray) -> np.ndarray:
+    s = np.ascontiguousarray(s, np.float32)
+    out = np.zeros(s.size, np.uint8)
+    _lib().ora_e4m3_rn_n(_ptr(s), s.size, _ptr(out))
+    return out

@@ -306,7 +306,7 @@ static void load_block(const view_t *v, int64_t r, int64_t j, int rht, uint32_t 
 int ora_quantize(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                  int orient, int mode, int block2d, int per_row, int swizzled,
                  int rht, uint32_t sign_mask, uint64_t seed, uint64_t offset,
-                 int64_t r0, int64_t r1,
+                 int64_t r0, int64_t r1, const float *amax_in,
                  uint8_t *codes, uint8_t *scales, float *amax_out, float *gscale_out) {
     view_t v = {x, dtype, rows, cols, ld, orient};
     int64_t R = orient ? cols : rows, C = orient ? rows : cols;
@@ -319,9 +319,14 @@ int ora_quantize(const void *x, int dtype, int64_t rows, int64_t cols, int64_t l
     int64_t CS = C / 16;
     float y[16];
 
-    /* Global amax over the post-RHT values (per tensor: everything). */
+    /* Global amax over the post-RHT values (per tensor: everything), unless
+     * the caller supplies it (amax_in, per tensor only). */
     float g_tensor = 0.0f;
-    if (!per_row) {
+    if (!per_row && amax_in) {
+        amax_out[0] = amax_in[0];
+        g_tensor = global_scale_of(amax_in[0]);
+        gscale_out[0] = g_tensor;
+    } else if (!per_row) {
         uint32_t mb = 0;
         for (int64_t r = 0; r < R; r++)
             for (int64_t j = 0; j < CS; j++) {
@@ -442,4 +447,15 @@ int ora_amax(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld, i
     }
     if (!per_row) { amax_out[0] = u2f(mt); gscale_out[0] = global_scale_of(u2f(mt)); }
     return ORA_OK;
+}
+
+/* ------------------------------------------- array forms (for the tests) */
+void ora_e2m1_rne_n(const float *q, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = (uint8_t)ora_e2m1_rne(q[i]);
+}
+void ora_e2m1_sr_n(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = (uint8_t)ora_e2m1_sr(q[i], r[i]);
+}
+void ora_e4m3_rn_n(const float *s, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = (uint8_t)ora_e4m3_rn(s[i]);
 }

@@ -1,0 +1,221 @@
+// nvfp4_api.cu -- the C ABI of libnvfp4.so (declared in include/nvfp4.h).
+//
+// Every entry point validates all of its arguments before enqueuing anything,
+// then enqueues kernels on the caller's stream and returns without waiting.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4.h"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+int sm_count() {
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+}  // namespace nvfp4
+
+namespace {
+
+constexpr uint32_t kKnownFlags = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_BLOCK_2D | NVFP4_SCALE_PER_ROW |
+                                 NVFP4_SWIZZLED | NVFP4_AMAX_GIVEN;
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+constexpr int64_t kMaxElems = (int64_t)1 << 34;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t elem_size(int32_t dtype) { return dtype == NVFP4_IN_FP32 ? 4 : 2; }
+
+// Shape, stride and pointer checks shared by every entry point that reads X.
+nvfp4_status check_input(const nvfp4_input *in) {
+    if (!in) return NVFP4_ERR_INVALID_ARG;
+    if (in->dtype != NVFP4_IN_BF16 && in->dtype != NVFP4_IN_FP32) return NVFP4_ERR_INVALID_ARG;
+    if (in->rows < 0 || in->cols < 0 || in->rows >= kMaxDim || in->cols >= kMaxDim) return NVFP4_ERR_INVALID_ARG;
+    if (in->rows * in->cols > kMaxElems) return NVFP4_ERR_INVALID_ARG;
+    if (in->rows == 0 || in->cols == 0) return NVFP4_OK;
+    if (!in->x || !aligned(in->x, 16)) return NVFP4_ERR_INVALID_ARG;
+    if (in->ld < in->cols || (in->ld * elem_size(in->dtype)) % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+nvfp4::QArgs make_args(const nvfp4_input *in, const nvfp4_output *out, void *ws, uint32_t flags) {
+    nvfp4::QArgs a{};
+    a.x = in->x;
+    a.rows = in->rows;
+    a.cols = in->cols;
+    a.ld = in->ld;
+    a.codes_row = out->codes_row;
+    a.scales_row = out->scales_row;
+    a.codes_col = out->codes_col;
+    a.scales_col = out->scales_col;
+    a.amax = out->amax;
+    a.gscale = out->global_scale;
+    a.workspace = static_cast<uint32_t *>(ws);
+    a.swizzled = (flags & NVFP4_SWIZZLED) ? 1 : 0;
+    a.want_row = (flags & NVFP4_ROWWISE) ? 1 : 0;
+    a.want_col = (flags & NVFP4_COLWISE) ? 1 : 0;
+    return a;
+}
+
+nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht, uint16_t sign_mask,
+                      uint64_t seed, uint64_t offset, nvfp4_output *out, void *ws, void *stream) {
+    nvfp4_status st = check_input(in);
+    if (st != NVFP4_OK) return st;
+    if (!out || (flags & ~kKnownFlags)) return NVFP4_ERR_INVALID_ARG;
+    const bool want_row = flags & NVFP4_ROWWISE, want_col = flags & NVFP4_COLWISE;
+    const bool block2d = flags & NVFP4_BLOCK_2D, per_row = flags & NVFP4_SCALE_PER_ROW;
+    const bool given = flags & NVFP4_AMAX_GIVEN, swz = flags & NVFP4_SWIZZLED;
+    if (!want_row && !want_col) return NVFP4_ERR_INVALID_ARG;
+    if (block2d && (mode != nvfp4::MODE_RNE_ID || rht || per_row)) return NVFP4_ERR_UNSUPPORTED;
+    if (per_row && (want_col || given)) return NVFP4_ERR_UNSUPPORTED;
+    if (rht && want_row && want_col) return NVFP4_ERR_UNSUPPORTED;
+    if (rht && mode == nvfp4::MODE_4O6_ID) return NVFP4_ERR_UNSUPPORTED;
+    if ((want_row || block2d) && in->cols % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+    if ((want_col || block2d) && in->rows % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+    const bool empty = in->rows == 0 || in->cols == 0;
+    // an empty input has empty code and scale arrays, which may be NULL
+    if (!empty && want_row && (!out->codes_row || !out->scales_row || !aligned(out->codes_row, 8)))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!empty && want_col && (!out->codes_col || !out->scales_col || !aligned(out->codes_col, 8)))
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t n_scale = per_row ? in->rows : 1;
+    if (n_scale > 0 && (!out->amax || !out->global_scale)) return NVFP4_ERR_INVALID_ARG;
+    if (!per_row && !given && !empty && !ws) return NVFP4_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (empty) {
+        // nothing to encode; an empty tensor (or row) has amax 0 and scale 0
+        if (!given && n_scale > 0 && cudaMemsetAsync(out->amax, 0, n_scale * sizeof(float), s) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        if (n_scale > 0 && cudaMemsetAsync(out->global_scale, 0, n_scale * sizeof(float), s) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        return NVFP4_OK;
+    }
+
+    nvfp4::QArgs a = make_args(in, out, ws, flags);
+    a.sign_mask = sign_mask;
+    a.seed = seed;
+    a.offset = offset;
+    const bool fp32 = in->dtype == NVFP4_IN_FP32;
+    if (per_row) {
+        st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, mode, rht, s));
+    } else {
+        if (!given) {
+            st = cuda_status(nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col, s));
+            if (st != NVFP4_OK) return st;
+        }
+        if (block2d) {
+            st = cuda_status(nvfp4::launch_quant_2d(a, fp32, s));
+        } else {
+            if (want_row) st = cuda_status(nvfp4::launch_quant_row(a, fp32, mode, rht, s));
+            if (st == NVFP4_OK && want_col) st = cuda_status(nvfp4::launch_quant_col(a, fp32, mode, rht, s));
+        }
+    }
+    if (st != NVFP4_OK) return st;
+    if (swz) {
+        if (want_row) st = cuda_status(nvfp4::launch_scale_pad(out->scales_row, in->rows, in->cols / 16, s));
+        if (st == NVFP4_OK && want_col) st = cuda_status(nvfp4::launch_scale_pad(out->scales_col, in->cols, in->rows / 16, s));
+    }
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_workspace_bytes(void) { return 256; }
+
+size_t nvfp4_scale_bytes(int64_t rows_out, int64_t cols_out, uint32_t flags) {
+    if (rows_out < 0 || cols_out < 0) return 0;
+    const int64_t cs = cols_out / 16;
+    if (!(flags & NVFP4_SWIZZLED)) return (size_t)(rows_out * cs);
+    return (size_t)(((rows_out + 127) / 128 * 128) * ((cs + 3) / 4 * 4));
+}
+
+nvfp4_status nvfp4_amax(const nvfp4_input *in, uint32_t flags, int use_rht, uint16_t sign_mask,
+                        nvfp4_output *out, void *workspace, void *stream) {
+    (void)sign_mask;  // signs do not change magnitudes
+    nvfp4_status st = check_input(in);
+    if (st != NVFP4_OK) return st;
+    if (!out || !out->amax || !out->global_scale) return NVFP4_ERR_INVALID_ARG;
+    if (flags & ~(uint32_t)(NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SCALE_PER_ROW)) return NVFP4_ERR_INVALID_ARG;
+    const bool col = (flags & NVFP4_COLWISE) && !(flags & NVFP4_ROWWISE);
+    const bool per_row = flags & NVFP4_SCALE_PER_ROW;
+    if (per_row && col) return NVFP4_ERR_UNSUPPORTED;
+    if ((per_row || (use_rht && !col)) && in->cols % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+    if (use_rht && col && in->rows % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+    const bool empty = in->rows == 0 || in->cols == 0;
+    if (!per_row && !empty && !workspace) return NVFP4_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (empty) {
+        const int64_t n = per_row ? in->rows : 1;
+        if (n > 0 && (cudaMemsetAsync(out->amax, 0, n * sizeof(float), s) != cudaSuccess ||
+                      cudaMemsetAsync(out->global_scale, 0, n * sizeof(float), s) != cudaSuccess))
+            return NVFP4_ERR_CUDA;
+        return NVFP4_OK;
+    }
+    nvfp4::QArgs a = make_args(in, out, workspace, 0);
+    const bool fp32 = in->dtype == NVFP4_IN_FP32;
+    if (per_row) return cuda_status(nvfp4::launch_amax_rows(a, fp32, use_rht != 0, s));
+    return cuda_status(nvfp4::launch_amax_tensor(a, fp32, use_rht != 0, col, s));
+}
+
+nvfp4_status nvfp4_quantize_rne(const nvfp4_input *in, uint32_t flags, nvfp4_output *out, void *workspace,
+                                void *stream) {
+    return quantize(in, flags, nvfp4::MODE_RNE_ID, false, 0, 0, 0, out, workspace, stream);
+}
+
+nvfp4_status nvfp4_quantize_sr(const nvfp4_input *in, uint32_t flags, uint64_t seed, uint64_t offset,
+                               nvfp4_output *out, void *workspace, void *stream) {
+    return quantize(in, flags, nvfp4::MODE_SR_ID, false, 0, seed, offset, out, workspace, stream);
+}
+
+nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16_t sign_mask, uint64_t seed,
+                                   uint64_t offset, nvfp4_output *out, void *workspace, void *stream) {
+    if ((flags & NVFP4_ROWWISE) && (flags & NVFP4_COLWISE)) return NVFP4_ERR_UNSUPPORTED;
+    return quantize(in, flags, nvfp4::MODE_SR_ID, true, sign_mask, seed, offset, out, workspace, stream);
+}
+
+nvfp4_status nvfp4_quantize_four_over_six(const nvfp4_input *in, uint32_t flags, nvfp4_output *out,
+                                          void *workspace, void *stream) {
+    return quantize(in, flags, nvfp4::MODE_4O6_ID, false, 0, 0, 0, out, workspace, stream);
+}
+
+nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *global_scale,
+                              int64_t rows, int64_t cols, uint32_t flags, void *out, int32_t out_dtype,
+                              void *stream) {
+    if (flags & ~(uint32_t)(NVFP4_SWIZZLED | NVFP4_SCALE_PER_ROW)) return NVFP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || rows >= kMaxDim || cols >= kMaxDim || rows * cols > kMaxElems || cols % 16 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_IN_BF16 && out_dtype != NVFP4_IN_FP32) return NVFP4_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return NVFP4_OK;
+    if (!codes || !scales || !global_scale || !out || !aligned(codes, 8) || !aligned(out, 16))
+        return NVFP4_ERR_INVALID_ARG;
+    return cuda_status(nvfp4::launch_dequant(codes, scales, global_scale, rows, cols,
+                                             (flags & NVFP4_SWIZZLED) ? 1 : 0, (flags & NVFP4_SCALE_PER_ROW) ? 1 : 0,
+                                             out, out_dtype == NVFP4_IN_FP32, static_cast<cudaStream_t>(stream)));
+}
+
+const char *nvfp4_status_string(nvfp4_status status) {
+    switch (status) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+        case NVFP4_ERR_UNSUPPORTED: return "unsupported combination";
+        case NVFP4_ERR_CUDA: return "CUDA error";
+        case NVFP4_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

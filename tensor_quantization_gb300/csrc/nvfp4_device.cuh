@@ -1,0 +1,229 @@
+// nvfp4_device.cuh -- sm_103a device primitives of the NVFP4 quantizer.
+//
+// Rounding-critical steps use explicit instructions so that no compiler
+// lowering choice can change a result: the hardware E4M3/E2M1 casts
+// (cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32) and their exact decodes, an exactly
+// rounded division, and fixed butterfly / reduction orders.
+// ("[nvfp4 training][rl] Add a CuTe DSL fast-path kernel for four-over-six
+// quantize #4852", PR description.)
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------------ bits
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t mag_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+__device__ __forceinline__ float copy_sign(float mag, float sgn) {
+    return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(sgn) & 0x80000000u));
+}
+
+// ------------------------------------------------------ packed fp32 pairs
+// Blackwell executes two fp32 lanes per instruction (add/sub/mul/fma .f32x2).
+struct f2 { float x, y; };
+
+__device__ __forceinline__ unsigned long long pk(f2 a) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+__device__ __forceinline__ f2 upk(unsigned long long r) {
+    f2 a;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+    return a;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+__device__ __forceinline__ f2 mulrz2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("mul.rz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+    return upk(r);
+}
+
+// ------------------------------------------------------------------ E4M3
+// Round-to-nearest-even, saturating (+-inf -> +-448), NaN -> 0x7F.
+__device__ __forceinline__ uint32_t e4m3_rn(float s) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+    return r & 0xFFu;
+}
+
+// Exact value of an E4M3 byte (E4M3 is a subset of fp16).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    uint32_t h2;
+    uint16_t in = (uint16_t)(b & 0xFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    float f;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.f32.f16 %0, lo; }" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// ------------------------------------------------------------------ E2M1
+// Eight fp32 values -> eight RNE/satfinite E2M1 codes packed in a word,
+// element k in nibble k (low nibble first).
+__device__ __forceinline__ uint32_t e2m1x8(float q0, float q1, float q2, float q3, float q4, float q5,
+                                           float q6, float q7) {
+    uint32_t w;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(w)
+        : "f"(q0), "f"(q1), "f"(q2), "f"(q3), "f"(q4), "f"(q5), "f"(q6), "f"(q7));
+    return w;
+}
+
+// Exact fp32 values of the two codes in byte `b` (low nibble -> .x).
+__device__ __forceinline__ f2 e2m1x2_value(uint32_t b) {
+    uint32_t h2;
+    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(b & 0xFFu));
+    f2 v;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }"
+        : "=f"(v.x), "=f"(v.y) : "r"(h2));
+    return v;
+}
+
+// ------------------------------------------------- exactly rounded y / d
+// Per block, d = Sf * g is fixed, so the reciprocal is formed once as an
+// unevaluated sum rh + rl (rh = RN(1/d), rl = RN((1 - d*rh) * rh), the
+// remainder 1 - d*rh being exact by FMA).  Per element:
+//   q0 = RN(y*rh + RN(y*rl))  -- relative error < 2^-46, so q0 is a faithful
+//                                rounding of y/d;
+//   e  = y - q0*d             -- exact (remainder of a faithful quotient);
+//   q  = RN(q0 + e*rh)        -- equals RN(y/d) by Markstein's theorem
+//                                (Markstein 1990; Muller et al., Handbook of
+//                                Floating-Point Arithmetic, ch. on division).
+// Preconditions for the fast path: d in [2^-80, 2^100] (normal, with a
+// normal reciprocal) and |y/d| < 2^4; quotients below 2^-11 may be inexact
+// but stay below 2^-10 and keep their sign, which fixes their E2M1 code.  The
+// product y*0 loses the sign of y = -0, so callers copy y's sign.
+struct Recip {
+    float d, rh, rl;
+    bool fast;
+};
+
+__device__ __forceinline__ Recip make_recip(float d) {
+    Recip R;
+    R.d = d;
+    R.fast = (d >= 0x1p-80f) && (d <= 0x1p100f);  // false for NaN
+    R.rh = __frcp_rn(d);
+    float rem = __fmaf_rn(-d, R.rh, 1.0f);
+    R.rl = __fmul_rn(rem, R.rh);
+    return R;
+}
+
+__device__ __forceinline__ f2 div2_fast(f2 y, const Recip &R) {
+    const f2 rh{R.rh, R.rh}, rl{R.rl, R.rl}, nd{-R.d, -R.d};
+    f2 t = mul2(y, rl);
+    f2 q0 = fma2(y, rh, t);
+    f2 e = fma2(q0, nd, y);
+    f2 q = fma2(e, rh, q0);
+    return f2{copy_sign(q.x, y.x), copy_sign(q.y, y.y)};
+}
+
+// IEEE division for blocks outside the fast range; NaN becomes +8 (encodes
+// as +6) and infinities are clamped to +-8 (also encode as +-6).
+__device__ __forceinline__ float div_slow(float y, float d) {
+    float q = __fdiv_rn(y, d);
+    if (q != q) return 8.0f;
+    return fminf(fmaxf(q, -8.0f), 8.0f);
+}
+
+// --------------------------------------------------- stochastic rounding
+// Scaling |q| < 8 by 2^-126 (rounding toward zero) puts the E2M1 grid at the
+// floats whose low 22 bits are zero, subnormal step 0.5 included; adding the
+// dither (r + 0.5) * 2^14 to the bits and truncating gives
+//   up  <=>  (|q| - a)/(b - a) + (r + 0.5)/256 >= 1
+// (the truncation only drops bits below the 2^-13 step of the dither, which
+// cannot change a ">=" against it).  Returns the chosen grid value, signed.
+__device__ __forceinline__ f2 sr_round2(f2 q, uint32_t r0, uint32_t r1) {
+    f2 z = mulrz2(q, f2{0x1p-126f, 0x1p-126f});
+    uint32_t t0 = (__float_as_uint(z.x) + ((r0 << 14) | 0x2000u)) & 0xFFC00000u;
+    uint32_t t1 = (__float_as_uint(z.y) + ((r1 << 14) | 0x2000u)) & 0xFFC00000u;
+    return mul2(f2{__uint_as_float(t0), __uint_as_float(t1)}, f2{0x1p126f, 0x1p126f});
+}
+
+// ----------------------------------------------------------- Philox4x32-10
+// Salmon et al., "Parallel random numbers: as easy as 1, 2, 3" (SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int i = 0; i < 10; i++) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
+        c0 = n0;
+        c2 = n2;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+// Random bytes of block `blk`: key = seed, counter = (blk, offset).
+__device__ __forceinline__ uint4 block_random(uint64_t seed, uint64_t offset, uint64_t blk) {
+    return philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)offset, (uint32_t)(offset >> 32),
+                         (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ------------------------------------------------------------ 16-point RHT
+// Butterfly with strides 1, 2, 4, 8 (this order defines the rounding).  The
+// block is held as 8 pairs v[k] = (y[2k], y[2k+1]); the stride-1 stage works
+// inside a pair, the later stages on whole pairs with packed adds.
+__device__ __forceinline__ void fwht16(f2 (&v)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        float a = v[k].x, b = v[k].y;
+        v[k].x = __fadd_rn(a, b);
+        v[k].y = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            if ((k & h) == 0) {
+                f2 a = v[k], b = v[k + h];
+                v[k] = add2(a, b);
+                v[k + h] = sub2(a, b);
+            }
+        }
+    }
+}
+
+// Per-pair multipliers (+-0.25) from the sign mask: bit j -> element j.
+__device__ __forceinline__ f2 rht_mult(uint32_t mask, int k) {
+    return f2{((mask >> (2 * k)) & 1u) ? -0.25f : 0.25f, ((mask >> (2 * k + 1)) & 1u) ? -0.25f : 0.25f};
+}
+
+// -------------------------------------------------------------- layouts
+__device__ __forceinline__ int64_t swizzle_offset(int64_t r, int64_t j, int64_t cs_p) {
+    return ((r >> 7) * (cs_p >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (j & 3);
+}
+
+}  // namespace nvfp4

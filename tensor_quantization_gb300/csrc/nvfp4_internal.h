@@ -1,0 +1,50 @@
+// nvfp4_internal.h -- launch interface between the C ABI (nvfp4_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// Rounding modes (same values as the Mode enum of the kernels).
+enum { MODE_RNE_ID = 0, MODE_SR_ID = 1, MODE_4O6_ID = 2 };
+
+struct QArgs {
+    const void *x;
+    int64_t rows, cols, ld;  // of X
+    uint8_t *codes_row, *scales_row, *codes_col, *scales_col;
+    float *amax;          // per tensor: [1] (input to the quantize kernels); per row: [R_out]
+    float *gscale;        // written: [1] or [R_out]
+    uint32_t *workspace;  // [0] running max bits, [1] CTA ticket, [2] status
+    uint32_t sign_mask;
+    uint64_t seed, offset;
+    int swizzled;
+    int want_row, want_col;
+};
+
+// Device properties, cached per device.
+int sm_count();
+
+// ---- launchers (return cudaGetLastError() after the launch) ----
+// Per-tensor amax (optionally of RHT blocks along rows (col=0) or columns
+// (col=1)); writes a.amax[0], a.gscale[0] and resets the workspace.
+cudaError_t launch_amax_tensor(const QArgs &a, bool fp32, bool rht, bool col, cudaStream_t s);
+// Per-row amax of the rowwise orientation (one value per X row).
+cudaError_t launch_amax_rows(const QArgs &a, bool fp32, bool rht, cudaStream_t s);
+
+// Rowwise 1x16 quantize with a per-tensor scale (a.amax[0]).
+cudaError_t launch_quant_row(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+// Columnwise 1x16 quantize with a per-tensor scale.
+cudaError_t launch_quant_col(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+// 16x16 tiles, RNE, rowwise and/or columnwise from one read.
+cudaError_t launch_quant_2d(const QArgs &a, bool fp32, cudaStream_t s);
+// Rowwise with one global scale per row, amax and quantize in one pass.
+cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+// Zero the pad bytes of a swizzled scale array.
+cudaError_t launch_scale_pad(uint8_t *scales, int64_t rows_out, int64_t cs, cudaStream_t s);
+
+cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *gscale, int64_t rows,
+                           int64_t cols, int swizzled, int per_row, void *out, int out_fp32, cudaStream_t s);
+
+}  // namespace nvfp4

@@ -1,0 +1,123 @@
+// gpu_probes.cu -- test-only kernels that run the library's device primitives
+// on arrays, so the tests can compare them with the CPU oracle (casts) and
+// with CUDA's own IEEE division.  Compiled by tests/test_gpu_primitives.py.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4_device.cuh"
+
+using namespace nvfp4;
+
+__global__ void k_e2m1(const float *q, int64_t n, uint8_t *out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    // element 0 of the packed word = low nibble; feed q twice to also check
+    // that element 1 lands in the high nibble
+    uint32_t w = e2m1x8(q[i], q[i], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
+    uint32_t lo = w & 15u, hi = (w >> 4) & 15u;
+    out[i] = (lo == hi) ? (uint8_t)lo : (uint8_t)0xFF;
+}
+
+__global__ void k_e2m1_order(uint32_t *out) {
+    // eight distinct values: codes 1..7 and 0x9 must appear in element order
+    out[0] = e2m1x8(0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f, -0.5f);
+}
+
+__global__ void k_sr(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    f2 v = sr_round2(f2{q[i], 0.f}, r[i], 0u);
+    out[i] = (uint8_t)(e2m1x8(v.x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 15u);
+}
+
+__global__ void k_e4m3(const float *s, int64_t n, uint8_t *out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i < n) out[i] = (uint8_t)e4m3_rn(s[i]);
+}
+
+__global__ void k_e4m3_value(float *out) { out[threadIdx.x] = e4m3_value(threadIdx.x); }
+
+__global__ void k_e2m1_value(float *out) {
+    f2 v = e2m1x2_value(threadIdx.x);
+    out[2 * threadIdx.x] = v.x;
+    out[2 * threadIdx.x + 1] = v.y;
+}
+
+__device__ __forceinline__ uint32_t mix(uint64_t x) {
+    x ^= x >> 33; x *= 0xff51afd7ed558ccdull; x ^= x >> 33; x *= 0xc4ceb9fe1a85ec53ull; x ^= x >> 33;
+    return (uint32_t)x;
+}
+
+// Exact division: the library's per-block path (fast when the reciprocal
+// range allows, IEEE otherwise) against __fdiv_rn.  Kinds: 0 random
+// significands, 1 near-midpoint quotients (y = RN(d*m), m a midpoint),
+// 2 random d over the whole fast range.  Quotients below 2^-11 only need to
+// stay below 2^-10 with the right sign.
+__global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *bad, float *first) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    uint32_t a = mix(seed * 0x9E3779B97F4A7C15ull + 2 * i), b = mix(seed ^ (0xD1B54A32D192ED03ull * (2 * i + 1)));
+    float d, y;
+    if (kind == 2) {
+        d = __uint_as_float(((mix(a) % 180u) + 47u) << 23 | (b & 0x7FFFFFu));   // 2^-80 .. 2^100
+    } else {
+        d = __uint_as_float((127u << 23) | (b & 0x7FFFFFu)) * __uint_as_float(((a >> 27) + 112u) << 23);
+    }
+    if (kind == 1) {
+        // m = the midpoint between a float f in [1, 2) and its successor (not an
+        // fp32 value), scaled by 2^k, k in [-12, 3]; y = RN(d * m) puts y / d
+        // close to m, often within far less than an ulp.  Every third pair
+        // uses d = 1 + j * 2^-23 (few significant bits), which makes d * m
+        // nearly representable more often.
+        if (a % 3u == 0u) d = 1.0f + (float)(b & 63u) * 0x1p-23f;
+        const double m = ((double)__uint_as_float((127u << 23) | (a & 0x7FFFFFu)) + 0x1p-24) *
+                         (double)__uint_as_float((uint32_t)(115 + (mix(b) & 15u)) << 23);
+        y = __double2float_rn((double)d * m);
+    } else {
+        float q = __uint_as_float((127u << 23) | (a & 0x7FFFFFu)) * __uint_as_float((uint32_t)(112 + (b >> 28)) << 23);
+        y = __fmul_rn(d, q);
+    }
+    if (a & 1u) y = -y;
+    const Recip R = make_recip(d);
+    f2 q = R.fast ? div2_fast(f2{y, y}, R) : f2{div_slow(y, d), div_slow(y, d)};
+    const float ref = __fdiv_rn(y, d);
+    bool ok;
+    if (fabsf(ref) < 0x1p-11f) ok = fabsf(q.x) < 0x1p-10f && signbit(q.x) == signbit(ref);
+    else ok = __float_as_uint(q.x) == __float_as_uint(fminf(fmaxf(ref, -8.f), 8.f)) || fabsf(ref) >= 8.f;
+    ok = ok && __float_as_uint(q.x) == __float_as_uint(q.y);
+    if (!ok) {
+        unsigned long long k = atomicAdd(bad, 1ull);
+        if (k < 4) { first[3 * k] = y; first[3 * k + 1] = d; first[3 * k + 2] = q.x; }
+    }
+}
+
+extern "C" {
+int probe_e2m1(const float *q, int64_t n, uint8_t *out) {
+    k_e2m1<<<(unsigned)((n + 255) / 256), 256>>>(q, n, out);
+    return cudaDeviceSynchronize();
+}
+int probe_e2m1_order(uint32_t *out) {
+    k_e2m1_order<<<1, 1>>>(out);
+    return cudaDeviceSynchronize();
+}
+int probe_sr(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
+    k_sr<<<(unsigned)((n + 255) / 256), 256>>>(q, r, n, out);
+    return cudaDeviceSynchronize();
+}
+int probe_e4m3(const float *s, int64_t n, uint8_t *out) {
+    k_e4m3<<<(unsigned)((n + 255) / 256), 256>>>(s, n, out);
+    return cudaDeviceSynchronize();
+}
+int probe_e4m3_value(float *out) {
+    k_e4m3_value<<<1, 256>>>(out);
+    return cudaDeviceSynchronize();
+}
+int probe_e2m1_value(float *out) {
+    k_e2m1_value<<<1, 256>>>(out);
+    return cudaDeviceSynchronize();
+}
+int probe_div(uint64_t seed, int64_t n, int kind, unsigned long long *bad, float *first) {
+    k_div<<<(unsigned)((n + 255) / 256), 256>>>(seed, n, kind, bad, first);
+    return cudaDeviceSynchronize();
+}
+}

@@ -1,0 +1,369 @@
+"""GPU parity: the sm_103a library (through its C ABI) against the CPU oracle.
+
+Codes, scales (pad bytes included) and the amax / global scale must be
+bit-identical.  Small cases span several tiles and ragged tails; the five
+workloads also run at full size, in the same call ``bench.py`` times.
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_quantization_gb300 import nvfp4
+from tensor_quantization_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tensor_quantization_gb300 import build
+    build.build()
+    nvfp4.load()
+
+
+def np_bits(x: torch.Tensor) -> np.ndarray:
+    x = x.contiguous()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16)
+    return x.numpy()
+
+
+def same_float_bits(a, b) -> bool:
+    a = np.asarray(a, np.float32).ravel()
+    b = np.asarray(b, np.float32).ravel()
+    if a.shape != b.shape:
+        return False
+    both_nan = np.isnan(a) & np.isnan(b)
+    return bool(np.all(both_nan | (a.view(np.uint32) == b.view(np.uint32))))
+
+
+def to_device(x_cpu: torch.Tensor) -> torch.Tensor:
+    """Device copy whose row pitch is a multiple of 16 bytes (the ABI's rule)."""
+    R, C = x_cpu.shape
+    per16 = 16 // x_cpu.element_size()
+    ld = (C + per16 - 1) // per16 * per16
+    if ld == C or R <= 1:
+        return x_cpu.cuda()
+    buf = torch.zeros(R, ld, dtype=x_cpu.dtype, device="cuda")
+    buf[:, :C] = x_cpu.cuda()
+    return buf[:, :C]
+
+
+def gpu_run(x_cpu: torch.Tensor, x_dev: torch.Tensor | None = None, **kw) -> dict:
+    x = to_device(x_cpu) if x_dev is None else x_dev
+    q = nvfp4.quantize(x, **kw)
+    torch.cuda.synchronize()
+    out = {}
+    for k in ("codes_row", "scales_row", "codes_col", "scales_col", "amax", "global_scale"):
+        t = getattr(q, k)
+        out[k] = None if t is None else t.cpu().numpy()
+    return out
+
+
+def oracle_run(x_cpu: torch.Tensor, *, mode="rne", rowwise=True, colwise=False, block2d=False, per_row=False,
+               swizzled=False, rht=False, sign_mask=0, seed=0, offset=0, amax=None, row_range=None) -> dict:
+    xn = np_bits(x_cpu)
+    kw = dict(mode=mode, block2d=block2d, per_row=per_row, swizzled=swizzled, rht=rht, sign_mask=sign_mask,
+              seed=seed, offset=offset, row_range=row_range,
+              amax_given=None if amax is None else float(amax))
+    out = {}
+    for orient, on in (("row", rowwise), ("col", colwise)):
+        if not on:
+            continue
+        o = oracle.quantize(xn, colwise=(orient == "col"), **kw)
+        out[f"codes_{orient}"] = o["codes"]
+        out[f"scales_{orient}"] = o["scales"].ravel()
+        out["amax"], out["global_scale"] = o["amax"], o["global_scale"]
+    return out
+
+
+def assert_parity(g: dict, o: dict, rows_sampled=None):
+    for k in ("codes_row", "scales_row", "codes_col", "scales_col"):
+        if k not in o:
+            continue
+        a, b = g[k], o[k]
+        if rows_sampled is not None and k.startswith("codes"):
+            a, b = a[rows_sampled], b[rows_sampled]
+        assert a.shape == b.shape, k
+        bad = np.argwhere(a.reshape(b.shape) != b)
+        assert bad.size == 0, f"{k}: {len(bad)} mismatches, first at {bad[:5].tolist()}"
+    assert same_float_bits(g["amax"], o["amax"]), (g["amax"][:4], o["amax"][:4])
+    assert same_float_bits(g["global_scale"], o["global_scale"]), (g["global_scale"][:4], o["global_scale"][:4])
+
+
+def mixed_input(rows, cols, seed, dtype=torch.bfloat16):
+    """Gaussian rows with log-uniform scales, exact zeros, -0 and outliers."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g) * torch.exp(torch.rand(rows, 1, generator=g) * 6 - 3)
+    x[torch.rand(rows, cols, generator=g) < 0.02] = 0.0
+    x[torch.rand(rows, cols, generator=g) < 0.01] = -0.0
+    x[torch.rand(rows, cols, generator=g) < 0.002] *= 300.0
+    return x.to(dtype)
+
+
+# ------------------------------------------------------ the five workloads
+SMALL = {
+    "randn_rne_256x1024": (256, 1024),
+    "act_rht_sr_8192x4096": (520, 1024),
+    "weight_2d_rne_14336x4096": (272, 512),
+    "grad_col_rht_sr_16384x8192": (256, 520),
+    "rowscaled_4o6_8192x8192": (96, 1024),
+}
+
+
+def workload_kwargs(w: wl.Workload, mask: int) -> dict:
+    return dict(mode=w.mode, rowwise=w.rowwise, colwise=w.colwise, block2d=w.block2d, per_row=w.per_row,
+                swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_workload_small(name):
+    w = wl.WORKLOADS[name].resized(*SMALL[name])
+    x, mask = wl.make_input(w)
+    kw = workload_kwargs(w, mask)
+    assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+def bands(n: int) -> list[tuple[int, int]]:
+    return [(0, 256), (n // 2 - 128, n // 2 + 128), (n - 256, n)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_workload_full_size(name):
+    """Full-size workloads through the call bench.py times.  Workloads up to the
+    headline size compare every output; larger ones compare bands of output
+    rows spread over the tensor (the per-tensor amax always covers all of it)
+    plus, for swizzled layouts, every scale byte."""
+    w = wl.WORKLOADS[name]
+    x, mask = wl.make_input(w)
+    kw = workload_kwargs(w, mask)
+    g = gpu_run(x, **kw)
+    if w.numel <= 8192 * 4096:
+        assert_parity(g, oracle_run(x, **kw))
+        return
+    for orient in ("row", "col"):
+        if not (w.rowwise if orient == "row" else w.colwise):
+            continue
+        R_out, C_out = (w.rows, w.cols) if orient == "row" else (w.cols, w.rows)
+        okw = dict(kw, rowwise=orient == "row", colwise=orient == "col")
+        for r0, r1 in bands(R_out):
+            o = oracle_run(x, row_range=(r0, r1), **okw)
+            ck, sk = f"codes_{orient}", f"scales_{orient}"
+            assert np.array_equal(g[ck][r0:r1], o[ck][r0:r1]), (name, ck, r0)
+            if not w.swizzled:
+                assert np.array_equal(g[sk].reshape(R_out, -1)[r0:r1], o[sk].reshape(R_out, -1)[r0:r1])
+            if w.per_row:
+                assert same_float_bits(g["amax"][r0:r1], o["amax"][r0:r1])
+                assert same_float_bits(g["global_scale"][r0:r1], o["global_scale"][r0:r1])
+            else:
+                assert same_float_bits(g["amax"], o["amax"])
+                assert same_float_bits(g["global_scale"], o["global_scale"])
+        if w.swizzled:
+            o = oracle_run(x, **okw)
+            assert np.array_equal(g[f"scales_{orient}"], o[f"scales_{orient}"]), name
+    if w.block2d:
+        # 2D: the column codes are the nibble transpose of the row codes
+        cr, cc = g["codes_row"], g["codes_col"]
+        ur = np.stack([cr & 15, cr >> 4], -1).reshape(cr.shape[0], -1)
+        uc = np.stack([cc & 15, cc >> 4], -1).reshape(cc.shape[0], -1)
+        assert np.array_equal(ur.T, uc)
+
+
+# ----------------------------------------------------- the option matrix
+MODES = ["rne", "sr", "rht_sr", "4o6"]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("swizzled", [False, True], ids=["linear", "swizzled"])
+@pytest.mark.parametrize("orient", ["row", "col", "both"])
+@pytest.mark.parametrize("mode", MODES)
+def test_option_matrix(mode, orient, swizzled, dtype):
+    if mode == "rht_sr" and orient == "both":
+        pytest.skip("the RHT path takes one orientation per call")
+    x = mixed_input(160, 208, seed=zlib.crc32(f"{mode}{orient}{swizzled}{dtype}".encode()) & 0xFFFF, dtype=dtype)
+    kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", rowwise=orient in ("row", "both"),
+              colwise=orient in ("col", "both"), swizzled=swizzled, sign_mask=0xB4E1, seed=77, offset=5)
+    assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("swizzled", [False, True], ids=["linear", "swizzled"])
+@pytest.mark.parametrize("mode", MODES)
+def test_per_row(mode, swizzled, dtype):
+    x = mixed_input(40, 336, seed=7, dtype=dtype)
+    kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", per_row=True, swizzled=swizzled,
+              sign_mask=0x0F0F, seed=3, offset=11)
+    assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("swizzled", [False, True], ids=["linear", "swizzled"])
+def test_2d_tiles(swizzled, dtype):
+    x = mixed_input(144, 240, seed=9, dtype=dtype)
+    for orient in ("row", "col", "both"):
+        kw = dict(mode="rne", block2d=True, rowwise=orient != "col", colwise=orient != "row", swizzled=swizzled)
+        assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+# ----------------------------------------------------------- edge cases
+def test_single_block_and_tiny_shapes():
+    for rows, cols, kw in [(1, 16, dict(mode="rne")), (16, 1, dict(mode="sr", rowwise=False, colwise=True)),
+                           (1, 16, dict(mode="sr", rht=True, sign_mask=0xFFFF, seed=2)),
+                           (16, 16, dict(mode="rne", block2d=True, colwise=True)),
+                           (1, 32, dict(mode="4o6", per_row=True)), (16, 3, dict(mode="rne", rowwise=False,
+                                                                                  colwise=True, swizzled=True))]:
+        x = mixed_input(rows, cols, seed=rows * 100 + cols)
+        assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+def test_zeros_and_signed_zeros():
+    for fill in (0.0, -0.0):
+        x = torch.full((32, 64), fill, dtype=torch.bfloat16)
+        for kw in (dict(mode="rne"), dict(mode="sr", rht=True, seed=1), dict(mode="4o6", per_row=True)):
+            g, o = gpu_run(x, **kw), oracle_run(x, **kw)
+            assert_parity(g, o)
+            assert np.all(g["codes_row"] == 0) and g["amax"][0] == 0
+
+
+def test_negative_zero_inside_a_block_keeps_its_sign():
+    x = torch.zeros(2, 32)
+    x[:, 0] = 3.0
+    x[:, 1] = -0.0
+    x[:, 2] = -1e-6
+    x = x.to(torch.bfloat16)
+    for kw in (dict(mode="rne"), dict(mode="sr", seed=4), dict(mode="4o6")):
+        g, o = gpu_run(x, **kw), oracle_run(x, **kw)
+        assert_parity(g, o)
+        assert (g["codes_row"][0, 0] >> 4) == 8  # element 1 = -0 -> code 0x8
+
+
+@pytest.mark.parametrize("special", ["nan", "inf", "-inf"])
+def test_nan_inf_policy(special):
+    x = mixed_input(64, 128, seed=12)
+    x[17, 45] = float(special)
+    for kw in (dict(mode="rne"), dict(mode="sr", rht=True, seed=5), dict(mode="4o6", per_row=True),
+               dict(mode="rne", block2d=True, colwise=True), dict(mode="sr", rowwise=False, colwise=True)):
+        assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+@pytest.mark.parametrize("scale", [1e-39, 1e-30, 1e30, 3e38])
+def test_extreme_magnitudes_take_the_exact_slow_path(scale):
+    x = (mixed_input(48, 96, seed=13, dtype=torch.float32) * scale)
+    x = torch.nan_to_num(x, posinf=3.4e38, neginf=-3.4e38)
+    for kw in (dict(mode="rne"), dict(mode="sr", seed=9), dict(mode="4o6"), dict(mode="4o6", per_row=True),
+               dict(mode="sr", rht=True, seed=1)):
+        assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+def test_subnormal_bf16_inputs():
+    bits = torch.randint(1, 0x0080, (32, 64), generator=torch.Generator().manual_seed(3), dtype=torch.int32)
+    sign = torch.randint(0, 2, (32, 64), generator=torch.Generator().manual_seed(4), dtype=torch.int32) << 15
+    x = (bits | sign).to(torch.int16).view(torch.bfloat16)
+    for kw in (dict(mode="rne"), dict(mode="sr", seed=2), dict(mode="4o6"), dict(mode="sr", rht=True, seed=2)):
+        assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+def test_strided_input_rows():
+    base = mixed_input(64, 208, seed=14)
+    x_dev = base.cuda()[:, 16:192]  # ld = 208 elements, cols = 176
+    x_cpu = base[:, 16:192].contiguous()
+    for kw in (dict(mode="rne"), dict(mode="sr", rht=True, seed=8), dict(mode="rne", colwise=True),
+               dict(mode="4o6", per_row=True), dict(mode="rne", block2d=True, colwise=True)):
+        assert_parity(gpu_run(x_cpu, x_dev=x_dev, **kw), oracle_run(x_cpu, **kw))
+
+
+def test_amax_given():
+    x = mixed_input(64, 256, seed=15)
+    for A in (float(x.float().abs().max()), 7.25, 1e-3):
+        for kw in (dict(mode="rne"), dict(mode="sr", seed=1, swizzled=True), dict(mode="4o6", colwise=True)):
+            g = gpu_run(x, amax=torch.tensor([A]).cuda(), **kw)
+            assert_parity(g, oracle_run(x, amax=A, **kw))
+
+
+def test_empty_inputs():
+    for shape in ((0, 32), (16, 0), (0, 0)):
+        x = torch.zeros(*shape, dtype=torch.bfloat16, device="cuda")
+        q = nvfp4.quantize(x, mode="rne", rowwise=shape[1] % 16 == 0, colwise=shape[1] % 16 != 0)
+        torch.cuda.synchronize()
+        assert float(q.amax[0]) == 0.0 and float(q.global_scale[0]) == 0.0
+
+
+def test_repeated_calls_reuse_the_workspace_and_offsets_change_draws():
+    x = mixed_input(128, 256, seed=16)
+    kw = dict(mode="sr", rht=True, sign_mask=0x1234, seed=10)
+    a = gpu_run(x, offset=0, **kw)
+    b = gpu_run(x, offset=0, **kw)
+    c = gpu_run(x, offset=1, **kw)
+    for k in ("codes_row", "scales_row", "amax"):
+        assert np.array_equal(a[k], b[k])
+    assert not np.array_equal(a["codes_row"], c["codes_row"])
+    assert_parity(c, oracle_run(x, offset=1, **kw))
+    ws = nvfp4.Workspace.get(torch.device("cuda"))
+    assert int(ws.view(torch.int32)[:2].abs().sum()) == 0  # returned to zero
+
+
+def test_non_default_stream():
+    x = mixed_input(256, 512, seed=17).cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        q = nvfp4.quantize(x, mode="sr", rht=True, sign_mask=5, seed=1, swizzled=True)
+    s.synchronize()
+    o = oracle_run(x.cpu(), mode="sr", rht=True, sign_mask=5, seed=1, swizzled=True)
+    assert np.array_equal(q.codes_row.cpu().numpy(), o["codes_row"])
+
+
+def test_amax_entry_point():
+    x = mixed_input(96, 128, seed=18)
+    xd = x.cuda()
+    for flags, rht in ((nvfp4.ROWWISE, False), (nvfp4.ROWWISE, True), (nvfp4.COLWISE, True),
+                       (nvfp4.ROWWISE | nvfp4.SCALE_PER_ROW, True), (nvfp4.ROWWISE | nvfp4.SCALE_PER_ROW, False)):
+        per_row = bool(flags & nvfp4.SCALE_PER_ROW)
+        n = 96 if per_row else 1
+        a = torch.empty(n, device="cuda")
+        gsc = torch.empty(n, device="cuda")
+        nvfp4.nvfp4_amax(xd, flags, rht, 0xFFFF, nvfp4.make_output(amax=a, global_scale=gsc),
+                         nvfp4.Workspace.get(xd.device))
+        torch.cuda.synchronize()
+        oa, og = oracle.amax(np_bits(x), colwise=bool(flags & nvfp4.COLWISE), rht=rht, per_row=per_row)
+        assert same_float_bits(a.cpu().numpy(), oa) and same_float_bits(gsc.cpu().numpy(), og)
+
+
+# ------------------------------------------------------------ dequantize
+@pytest.mark.parametrize("swizzled", [False, True])
+@pytest.mark.parametrize("per_row", [False, True])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_dequantize(swizzled, per_row, out_dtype):
+    x = mixed_input(200, 96, seed=19)
+    x[3, 5] = float("nan")
+    o = oracle.quantize(np_bits(x), mode="4o6" if per_row else "sr", per_row=per_row, swizzled=swizzled, seed=2)
+    ref = oracle.dequantize(o["codes"], o["scales"], o["global_scale"], 200, 96, swizzled=swizzled,
+                            per_row=per_row, out_dtype="bf16" if out_dtype == torch.bfloat16 else "fp32")
+    got = nvfp4.dequantize(torch.from_numpy(o["codes"]).cuda(), torch.from_numpy(o["scales"].ravel()).cuda(),
+                           torch.from_numpy(o["global_scale"]).cuda(), 200, 96, swizzled=swizzled,
+                           per_row=per_row, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    if out_dtype == torch.bfloat16:
+        g = got.cpu().view(torch.int16).numpy().view(np.uint16)
+        nan_g = (g & 0x7FFF) > 0x7F80
+        nan_r = (ref & 0x7FFF) > 0x7F80
+        assert np.array_equal(nan_g, nan_r)
+        assert np.array_equal(g[~nan_g], ref[~nan_r])
+    else:
+        assert same_float_bits(got.cpu().numpy(), ref)
+
+
+def test_round_trip_through_the_library():
+    x = mixed_input(128, 256, seed=20)
+    q = nvfp4.quantize(x.cuda(), mode="rne", swizzled=True)
+    d = nvfp4.dequantize(q.codes_row, q.scales_row, q.global_scale, 128, 256, swizzled=True)
+    torch.cuda.synchronize()
+    err = (d.cpu() - x.float()).abs()
+    assert math.isfinite(float(err.max()))
+    assert float((err <= x.float().abs() * 0.25 + 1e-3 * x.float().abs().max()).float().mean()) > 0.99

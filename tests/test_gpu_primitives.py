@@ -1,0 +1,136 @@
+"""The library's device primitives on the GPU, one at a time.
+
+The hardware casts (cvt.rn.satfinite.e2m1x2 / e4m3x2 and their decodes) are
+checked against the oracle's converters over dense sweeps of every binade they
+can see, which also fixes operand order, nibble order, NaN, -0 and
+saturation.  The per-block exact division is checked against CUDA's own IEEE
+division on random and near-midpoint quotients.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.fixture(scope="module")
+def probes(tmp_path_factory):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tensor_quantization_gb300 import build
+    so = str(tmp_path_factory.mktemp("probes") / "libprobes.so")
+    subprocess.run([build.nvcc(), *build.ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+                    "-I", build.CSRC, os.path.join(HERE, "gpu_probes.cu"), "-o", so], check=True)
+    torch.zeros(1, device="cuda")  # create the context first
+    lib = ctypes.CDLL(so)
+    vp, i64, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
+    lib.probe_e2m1.argtypes = [vp, i64, vp]
+    lib.probe_e2m1_order.argtypes = [vp]
+    lib.probe_sr.argtypes = [vp, vp, i64, vp]
+    lib.probe_e4m3.argtypes = [vp, i64, vp]
+    lib.probe_e4m3_value.argtypes = [vp]
+    lib.probe_e2m1_value.argtypes = [vp]
+    lib.probe_div.argtypes = [u64, i64, i32, vp, vp]
+    return lib
+
+
+def ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def dense_floats(exp_lo, exp_hi, mant_bits, seed):
+    """Every sign, every binade 2^exp_lo..2^exp_hi, the top mant_bits of the
+    significand enumerated, the remaining bits random."""
+    rng = np.random.default_rng(seed)
+    e = np.arange(exp_lo + 127, exp_hi + 128, dtype=np.uint32)
+    top = np.arange(1 << mant_bits, dtype=np.uint32) << (23 - mant_bits)
+    grid = (e[:, None] << 23 | top[None, :]).ravel()
+    low = rng.integers(0, 1 << (23 - mant_bits), grid.size, dtype=np.uint32)
+    bits = np.concatenate([grid, grid | low, grid | ((1 << (23 - mant_bits)) - 1)])
+    bits = np.concatenate([bits, bits | 0x80000000])
+    return bits.view(np.float32)
+
+
+SPECIALS = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, -np.nan, 1e-45, -1e-45, 3.4e38, -3.4e38,
+                     0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 7.0, 448.0, 464.0, 480.0, 1e9],
+                    np.float32)
+
+
+def run_cast(fn, vals):
+    q = torch.from_numpy(vals).cuda()
+    out = torch.empty(vals.size, dtype=torch.uint8, device="cuda")
+    assert fn(ptr(q), vals.size, ptr(out)) == 0
+    return out.cpu().numpy()
+
+
+def test_e2m1_cast_matches_oracle(probes):
+    vals = np.concatenate([dense_floats(-24, 4, 12, 1), SPECIALS,
+                           np.random.default_rng(2).integers(0, 2 ** 32, 1 << 20, dtype=np.uint32).view(np.float32)])
+    got = run_cast(probes.probe_e2m1, vals)
+    ref = oracle.e2m1_rne_array(vals)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(vals[i]), int(got[i]), int(ref[i])) for i in bad[:8]]
+
+
+def test_e2m1_pack_order(probes):
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert probes.probe_e2m1_order(ptr(out)) == 0
+    w = int(out.item()) & 0xFFFFFFFF
+    assert [(w >> (4 * k)) & 15 for k in range(8)] == [1, 2, 3, 4, 5, 6, 7, 9]
+
+
+def test_sr_round_matches_oracle(probes):
+    rng = np.random.default_rng(3)
+    q = np.concatenate([dense_floats(-12, 3, 10, 4), SPECIALS[np.isfinite(SPECIALS)]])
+    q = q[np.abs(q) < 8.0]
+    q = np.repeat(q, 3)
+    r = rng.integers(0, 256, q.size, dtype=np.uint8)
+    qt, rt = torch.from_numpy(q).cuda(), torch.from_numpy(r).cuda()
+    out = torch.empty(q.size, dtype=torch.uint8, device="cuda")
+    assert probes.probe_sr(ptr(qt), ptr(rt), q.size, ptr(out)) == 0
+    got = out.cpu().numpy()
+    ref = oracle.e2m1_sr_array(q, r)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(q[i]), int(r[i]), int(got[i]), int(ref[i])) for i in bad[:8]]
+
+
+def test_e4m3_cast_matches_oracle(probes):
+    vals = np.concatenate([dense_floats(-12, 10, 12, 5), SPECIALS,
+                           np.random.default_rng(6).integers(0, 2 ** 32, 1 << 20, dtype=np.uint32).view(np.float32)])
+    got = run_cast(probes.probe_e4m3, vals)
+    ref = oracle.e4m3_rn_array(vals)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(vals[i]), int(got[i]), int(ref[i])) for i in bad[:8]]
+
+
+def test_decodes_match_oracle(probes):
+    out = torch.empty(256, device="cuda")
+    assert probes.probe_e4m3_value(ptr(out)) == 0
+    got = out.cpu().numpy()
+    for b in range(256):
+        ref = oracle.e4m3_value(b)
+        assert (np.isnan(got[b]) and np.isnan(ref)) or np.float32(ref).view(np.uint32) == got[b].view(np.uint32)
+    out = torch.empty(512, device="cuda")
+    assert probes.probe_e2m1_value(ptr(out)) == 0
+    got = out.cpu().numpy()
+    for b in range(256):
+        assert got[2 * b] == oracle.e2m1_value(b & 15) and got[2 * b + 1] == oracle.e2m1_value(b >> 4)
+        assert np.signbit(got[2 * b]) == bool(b & 8)
+
+
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_exact_division(probes, kind):
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    first = torch.zeros(12, device="cuda")
+    n = 1 << 26
+    for seed in range(8):
+        assert probes.probe_div(seed + 100 * kind, n, kind, ptr(bad), ptr(first)) == 0
+    assert int(bad.item()) == 0, first.cpu().numpy().reshape(-1, 3)[:4]
