@@ -55,19 +55,36 @@ __global__ void __launch_bounds__(256) k_amax_plain(const QArgs a) {
     publish_tensor_amax(a, m, false);
 }
 
-// RHT blocks along rows.
+// RHT blocks along rows.  Each CTA scans one contiguous range of blocks with
+// the next block's loads in flight while the current one is transformed.
 template <typename T>
 __global__ void __launch_bounds__(256) k_amax_rht_row(const QArgs a) {
     const uint32_t CS = (uint32_t)(a.cols >> 4);
     const uint32_t n = (uint32_t)a.rows * CS;
+    const uint32_t per = ((n + gridDim.x - 1) / gridDim.x + 31) & ~31u;
+    const uint32_t b0 = blockIdx.x * per, b1 = min(n, b0 + per);
     const T *x = static_cast<const T *>(a.x);
     uint32_t m = 0;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const uint32_t r = i / CS, j = i - r * CS;
-        f2 v[8];
-        load_block_row(x + (int64_t)r * a.ld + 16 * j, v);
-        fwht16(v);
-        m = max(m, amax_bits(v));
+    if (b0 < n) {
+        uint32_t i = b0 + threadIdx.x;
+        uint32_t r = i / CS, j = i - r * CS;
+        const uint32_t dr = blockDim.x / CS, dj = blockDim.x % CS;
+        RawBlock<T> cur, nxt;
+        if (i < b1) load_raw(x + (int64_t)r * a.ld + 16 * j, cur);
+        while (i < b1) {
+            uint32_t r2 = r + dr, j2 = j + dj;
+            if (j2 >= CS) { j2 -= CS; ++r2; }
+            const uint32_t i2 = i + blockDim.x;
+            if (i2 < b1) load_raw(x + (int64_t)r2 * a.ld + 16 * j2, nxt);
+            f2 v[8];
+            unpack(cur, v);
+            fwht16(v);
+            m = max(m, __float_as_uint(block_amax(v)));
+            i = i2;
+            r = r2;
+            j = j2;
+            cur = nxt;
+        }
     }
     publish_tensor_amax(a, m, true);
 }
@@ -95,7 +112,7 @@ __global__ void __launch_bounds__(256) k_amax_rht_col(const QArgs a) {
             for (int p = 0; p < 8; p++) v[p] = f2{rows[2 * p].get(cc), rows[2 * p + 1].get(cc)};
             fwht16(v);
             // columns past the edge were loaded as zeros and stay zero
-            m = max(m, amax_bits(v));
+            m = max(m, __float_as_uint(block_amax(v)));
         }
     }
     publish_tensor_amax(a, m, true);
@@ -113,7 +130,7 @@ __global__ void __launch_bounds__(256) k_amax_rows(const QArgs a) {
             f2 v[8];
             load_block_row(x + r * a.ld + 16 * j, v);
             if (RHT) fwht16(v);
-            m = max(m, amax_bits(v));
+            m = max(m, __float_as_uint(block_amax(v)));
         }
         m = block_max_u32(m, red);
         if (threadIdx.x == 0) {

@@ -17,8 +17,11 @@ namespace nvfp4 {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t mag_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
-__device__ __forceinline__ float copy_sign(float mag, float sgn) {
-    return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(sgn) & 0x80000000u));
+// max(|a|, |b|) that returns NaN if either is NaN.
+__device__ __forceinline__ float absmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)));
+    return r;
 }
 
 // ------------------------------------------------------ packed fp32 pairs
@@ -107,49 +110,63 @@ __device__ __forceinline__ f2 e2m1x2_value(uint32_t b) {
 }
 
 // ------------------------------------------------- exactly rounded y / d
-// Per block, d = Sf * g is fixed, so the reciprocal is formed once as an
-// unevaluated sum rh + rl (rh = RN(1/d), rl = RN((1 - d*rh) * rh), the
-// remainder 1 - d*rh being exact by FMA).  Per element:
-//   q0 = RN(y*rh + RN(y*rl))  -- relative error < 2^-46, so q0 is a faithful
-//                                rounding of y/d;
-//   e  = y - q0*d             -- exact (remainder of a faithful quotient);
-//   q  = RN(q0 + e*rh)        -- equals RN(y/d) by Markstein's theorem
-//                                (Markstein 1990; Muller et al., Handbook of
-//                                Floating-Point Arithmetic, ch. on division).
-// Preconditions for the fast path: d in [2^-80, 2^100] (normal, with a
-// normal reciprocal) and |y/d| < 2^4; quotients below 2^-11 may be inexact
-// but stay below 2^-10 and keep their sign, which fixes their E2M1 code.  The
-// product y*0 loses the sign of y = -0, so callers copy y's sign.
-struct Recip {
-    float d, rh, rl;
-    bool fast;
+// A block divides all of its elements by the same d = Sf * g, and d takes at
+// most 128 values per global scale, so the reciprocal is prepared once per d:
+//   rd = RD(1/d), rl = RN((1 - d*rd) * rd) >= 0  (the remainder 1 - d*rd is
+//   exact by FMA and non-negative), rh = RN(1/d).
+// Per element (two at a time, packed):
+//   q0 = RN(y*rd + RN(y*rl))   relative error < 2^-46: a faithful rounding of
+//                              y/d, with the sign of y even for y = -0
+//                              (both products carry y's sign);
+//   f  = y - q0*d              exact (remainder of a faithful quotient);
+//   q  = RN(q0 + f*rh)         = RN(y/d) by Markstein's theorem (Markstein
+//                              1990; Muller et al., Handbook of
+//                              Floating-Point Arithmetic, division chapter).
+// The sequence is evaluated on negated reciprocals and returns -q, which keeps
+// every signed zero exact without a sign fix-up; callers flip the code sign.
+// Fast-path precondition: d in [2^-80, 2^100], y finite.  Quotients below
+// 2^-11 may be inexact but stay below 2^-10 with the right sign, which fixes
+// their E2M1 code and their E4M3 rounding; a quotient that overflows becomes
+// +-inf, which both the saturating casts and sr_round2 encode as +-6.
+struct Divisor {
+    float d, nrh, nrd, nrl;  // d, -RN(1/d), -RD(1/d), -rl
 };
 
-__device__ __forceinline__ Recip make_recip(float d) {
-    Recip R;
-    R.d = d;
-    R.fast = (d >= 0x1p-80f) && (d <= 0x1p100f);  // false for NaN
-    R.rh = __frcp_rn(d);
-    float rem = __fmaf_rn(-d, R.rh, 1.0f);
-    R.rl = __fmul_rn(rem, R.rh);
-    return R;
+__device__ __forceinline__ Divisor make_divisor(float d) {
+    Divisor D;
+    D.d = d;
+    const float rd = __frcp_rd(d);
+    const float rem = __fmaf_rn(-d, rd, 1.0f);
+    D.nrh = -__frcp_rn(d);
+    D.nrd = -rd;
+    D.nrl = -__fmul_rn(rem, rd);
+    return D;
 }
 
-__device__ __forceinline__ f2 div2_fast(f2 y, const Recip &R) {
-    const f2 rh{R.rh, R.rh}, rl{R.rl, R.rl}, nd{-R.d, -R.d};
-    f2 t = mul2(y, rl);
-    f2 q0 = fma2(y, rh, t);
-    f2 e = fma2(q0, nd, y);
-    f2 q = fma2(e, rh, q0);
-    return f2{copy_sign(q.x, y.x), copy_sign(q.y, y.y)};
+__device__ __forceinline__ bool divisor_fast(float d) { return d >= 0x1p-80f && d <= 0x1p100f; }  // NaN: false
+
+// -RN(y/d) for two numerators (fast path).
+__device__ __forceinline__ f2 neg_quot2(f2 y, const Divisor &D) {
+    const f2 t = mul2(y, f2{D.nrl, D.nrl});
+    const f2 nq = fma2(y, f2{D.nrd, D.nrd}, t);
+    const f2 f = fma2(nq, f2{D.d, D.d}, y);
+    return fma2(f, f2{D.nrh, D.nrh}, nq);
 }
 
-// IEEE division for blocks outside the fast range; NaN becomes +8 (encodes
-// as +6) and infinities are clamped to +-8 (also encode as +-6).
-__device__ __forceinline__ float div_slow(float y, float d) {
-    float q = __fdiv_rn(y, d);
-    if (q != q) return 8.0f;
-    return fminf(fmaxf(q, -8.0f), 8.0f);
+// RN(a/d) for a > 0 (scalar, fast path).
+__device__ __forceinline__ float quot_pos(float a, const Divisor &D) {
+    const float nq = __fmaf_rn(a, D.nrd, __fmul_rn(a, D.nrl));
+    const float f = __fmaf_rn(nq, D.d, a);
+    return -__fmaf_rn(f, D.nrh, nq);
+}
+
+// -RN(y/d) by IEEE division for divisors outside the fast range, clamped to
+// [-8, 8] (every |q| >= 6 encodes as 6); NaN becomes -8 so that it encodes as
+// +6 once the code sign is flipped.
+__device__ __forceinline__ float neg_quot_slow(float y, float d) {
+    const float q = __fdiv_rn(y, d);
+    if (q != q) return -8.0f;
+    return -fminf(fmaxf(q, -8.0f), 8.0f);
 }
 
 // --------------------------------------------------- stochastic rounding

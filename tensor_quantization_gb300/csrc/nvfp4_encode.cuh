@@ -1,6 +1,10 @@
 // nvfp4_encode.cuh -- block-level encoders shared by the quantize kernels.
 //
 // A 1x16 block is held as 8 fp32 pairs (element 2k in .x, 2k+1 in .y).
+//
+// For one global scale g, the element divisor d = Sf * g takes one of 128
+// values (one per non-negative E4M3 byte), so each CTA prepares all of them
+// once (DivTable, in shared memory) and a block only looks its divisor up.
 #pragma once
 
 #include "nvfp4_device.cuh"
@@ -9,101 +13,136 @@ namespace nvfp4 {
 
 enum Mode { MODE_RNE = 0, MODE_SR = 1, MODE_4O6 = 2 };
 
-// Unsigned max of magnitude bits: max |v|, with NaN beating every number.
-__device__ __forceinline__ uint32_t amax_bits(const f2 (&v)[8]) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int k = 0; k < 8; k++) m = max(m, max(mag_bits(v[k].x), mag_bits(v[k].y)));
-    return m;
-}
-
 // Decode scale of the tensor / row: g = A / (6 * 448).
 __device__ __forceinline__ float global_scale_of(float A) { return __fdiv_rn(A, 2688.0f); }
 
-// S = e4m3(amax_b / (M * g)); an all-zero block gets 0.
+// max |v| over a block (NaN if any element is NaN).
+__device__ __forceinline__ float block_amax(const f2 (&v)[8]) {
+    float m0 = absmax_nan(v[0].x, v[0].y), m1 = absmax_nan(v[1].x, v[1].y);
+    float m2 = absmax_nan(v[2].x, v[2].y), m3 = absmax_nan(v[3].x, v[3].y);
+#pragma unroll
+    for (int k = 4; k < 8; k += 4) {
+        m0 = absmax_nan(m0, absmax_nan(v[k].x, v[k].y));
+        m1 = absmax_nan(m1, absmax_nan(v[k + 1].x, v[k + 1].y));
+        m2 = absmax_nan(m2, absmax_nan(v[k + 2].x, v[k + 2].y));
+        m3 = absmax_nan(m3, absmax_nan(v[k + 3].x, v[k + 3].y));
+    }
+    return absmax_nan(absmax_nan(m0, m1), absmax_nan(m2, m3));
+}
+
+// The 128 element divisors of one global scale.  Entry s holds
+// d = RN(value(s) * g) and its reciprocal pieces; entry 0x7F (NaN) has d = NaN
+// and takes the IEEE path.
+struct DivTable {
+    Divisor e[128];
+};
+
+__device__ __forceinline__ void build_table(DivTable &T, float g, int tid, int nthreads) {
+    for (int s = tid; s < 128; s += nthreads) T.e[s] = make_divisor(__fmul_rn(e4m3_value((uint32_t)s), g));
+}
+
+// Divisors M*g of the block-scale computation (M = 6, and 4 for four-over-six).
+struct ScaleDiv {
+    Divisor m6, m4;
+    bool fast6, fast4;
+};
+
+__device__ __forceinline__ ScaleDiv make_scale_div(float g) {
+    ScaleDiv s;
+    s.m6 = make_divisor(__fmul_rn(6.0f, g));
+    s.m4 = make_divisor(__fmul_rn(4.0f, g));
+    s.fast6 = divisor_fast(s.m6.d);
+    s.fast4 = divisor_fast(s.m4.d);
+    return s;
+}
+
+// S = e4m3(amax_b / (M * g)); an all-zero block gets 0; NaN gives 0x7F.
 // ("nvfp4-sm120" README, section "Layout": two-level E2M1/E4M3 scaling.)
-__device__ __forceinline__ uint32_t block_scale(uint32_t amax_b, float M, float g) {
-    if (amax_b == 0u) return 0u;
-    float dM = __fmul_rn(M, g);
-    return e4m3_rn(__fdiv_rn(__uint_as_float(amax_b), dM));
+__device__ __forceinline__ uint32_t block_scale(float amax_b, const Divisor &dm, bool fast) {
+    if (amax_b == 0.0f) return 0u;
+    return e4m3_rn(fast ? quot_pos(amax_b, dm) : __fdiv_rn(amax_b, dm.d));
 }
 
 // Random byte of element e (byte e&3 of word e>>2).
 __device__ __forceinline__ uint32_t rbyte(const uint4 &r, int e) {
-    uint32_t w = (e >> 2) == 0 ? r.x : (e >> 2) == 1 ? r.y : (e >> 2) == 2 ? r.z : r.w;
+    const uint32_t w = (e >> 2) == 0 ? r.x : (e >> 2) == 1 ? r.y : (e >> 2) == 2 ? r.z : r.w;
     return (w >> (8 * (e & 3))) & 0xFFu;
 }
 
-// Quotients q = y / (Sf * g) of one block (exactly rounded), then the E2M1
-// codes (RNE, or SR with the block's random bytes).  Returns 8 bytes of codes:
-// .x = elements 0..7, .y = elements 8..15.
+// E2M1 codes of one block against divisor D (S != 0): exactly rounded
+// quotients (negated, see neg_quot2), stochastic rounding when SR, the RN
+// cast, and one XOR per 8 codes to restore the sign.  .x = elements 0..7.
 template <bool SR>
-__device__ __forceinline__ uint2 encode_with_scale(const f2 (&y)[8], uint32_t S, float g, const uint4 &rnd) {
-    const float Sf = e4m3_value(S);
-    if (Sf == 0.0f) return make_uint2(0u, 0u);
-    const float d = __fmul_rn(Sf, g);
-    const Recip R = make_recip(d);
-    f2 q[8];
-    if (R.fast) {
+__device__ __forceinline__ uint2 encode_codes(const f2 (&y)[8], const Divisor &D, const uint4 &rnd) {
+    f2 nq[8];
+    if (divisor_fast(D.d)) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) q[k] = div2_fast(y[k], R);
+        for (int k = 0; k < 8; k++) nq[k] = neg_quot2(y[k], D);
     } else {
 #pragma unroll
-        for (int k = 0; k < 8; k++) q[k] = f2{div_slow(y[k].x, d), div_slow(y[k].y, d)};
+        for (int k = 0; k < 8; k++) nq[k] = f2{neg_quot_slow(y[k].x, D.d), neg_quot_slow(y[k].y, D.d)};
     }
     if (SR) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) q[k] = sr_round2(q[k], rbyte(rnd, 2 * k), rbyte(rnd, 2 * k + 1));
+        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], rbyte(rnd, 2 * k), rbyte(rnd, 2 * k + 1));
     }
     uint2 c;
-    c.x = e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
-    c.y = e2m1x8(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y);
+    c.x = e2m1x8(nq[0].x, nq[0].y, nq[1].x, nq[1].y, nq[2].x, nq[2].y, nq[3].x, nq[3].y) ^ 0x88888888u;
+    c.y = e2m1x8(nq[4].x, nq[4].y, nq[5].x, nq[5].y, nq[6].x, nq[6].y, nq[7].x, nq[7].y) ^ 0x88888888u;
     return c;
+}
+
+template <bool SR>
+__device__ __forceinline__ uint2 encode_with_scale(const f2 (&y)[8], uint32_t S, const DivTable &T,
+                                                   const uint4 &rnd) {
+    if (S == 0u) return make_uint2(0u, 0u);
+    return encode_codes<SR>(y, T.e[S & 0x7Fu], rnd);
 }
 
 // Four-over-six candidate error: squared dequantization error, reduced by
 // the clamped shuffle-down tree (offsets 8, 4, 2, 1: lane i += lane i+off).
-// (PR #4852 description: pinned width-16 error reduction.)
-__device__ __forceinline__ float candidate_error(const f2 (&y)[8], uint2 codes, uint32_t S, float g) {
-    const float Sf = e4m3_value(S);
-    const float d = (Sf == 0.0f) ? 0.0f : __fmul_rn(Sf, g);
-    const f2 dd{d, d};
-    f2 p[8];
+// (PR #4852 description: pinned width-16 error reduction.)  Every product and
+// sum is a separate, individually rounded scalar operation: ptxas may fuse a
+// packed f32x2 multiply into a following packed add, which would round
+// y - val*d once instead of twice and break the pinned error (and with it
+// ties between candidates that dequantize identically).  d = 0 when S = 0.
+__device__ __forceinline__ float candidate_error(const f2 (&y)[8], uint2 codes, float d) {
+    float p[16];
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         const uint32_t w = (k < 4) ? codes.x : codes.y;
         const f2 val = e2m1x2_value(w >> (8 * (k & 3)));
-        const f2 e = sub2(y[k], mul2(val, dd));
-        p[k] = mul2(e, e);
+        const float e0 = __fsub_rn(y[k].x, __fmul_rn(val.x, d));
+        const float e1 = __fsub_rn(y[k].y, __fmul_rn(val.y, d));
+        p[2 * k] = __fmul_rn(e0, e0);
+        p[2 * k + 1] = __fmul_rn(e1, e1);
     }
-    // pair k holds (p[2k], p[2k+1]); offset 8 pairs k with k+4, offset 4 with
-    // k+2, offset 2 with k+1, offset 1 is the final scalar add.
 #pragma unroll
-    for (int k = 0; k < 4; k++) p[k] = add2(p[k], p[k + 4]);
+    for (int off = 8; off >= 1; off >>= 1)
 #pragma unroll
-    for (int k = 0; k < 2; k++) p[k] = add2(p[k], p[k + 2]);
-    p[0] = add2(p[0], p[1]);
-    return __fadd_rn(p[0].x, p[0].y);
+        for (int i = 0; i < off; i++) p[i] = __fadd_rn(p[i], p[i + off]);
+    return p[0];
 }
 
 // Encode one block in the given mode.  Returns the codes and writes S.
 template <int MODE>
-__device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], float g, const uint4 &rnd, uint32_t &S_out) {
-    const uint32_t am = amax_bits(y);
+__device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &sd, const DivTable &T,
+                                              const uint4 &rnd, uint32_t &S_out) {
+    const float am = block_amax(y);
     if (MODE == MODE_4O6) {
-        const uint32_t S6 = block_scale(am, 6.0f, g);
-        const uint32_t S4 = block_scale(am, 4.0f, g);
-        const uint2 c6 = encode_with_scale<false>(y, S6, g, rnd);
-        const uint2 c4 = encode_with_scale<false>(y, S4, g, rnd);
-        const float e6 = candidate_error(y, c6, S6, g);
-        const float e4 = candidate_error(y, c4, S4, g);
+        const uint32_t S6 = block_scale(am, sd.m6, sd.fast6);
+        const uint32_t S4 = block_scale(am, sd.m4, sd.fast4);
+        const uint2 c6 = encode_with_scale<false>(y, S6, T, rnd);
+        const uint2 c4 = encode_with_scale<false>(y, S4, T, rnd);
+        const float e6 = candidate_error(y, c6, S6 ? T.e[S6 & 0x7Fu].d : 0.0f);
+        const float e4 = candidate_error(y, c4, S4 ? T.e[S4 & 0x7Fu].d : 0.0f);
         const bool pick4 = e4 < e6;  // ties and NaN keep map-to-6
         S_out = pick4 ? S4 : S6;
         return pick4 ? c4 : c6;
     } else {
-        const uint32_t S = block_scale(am, 6.0f, g);
+        const uint32_t S = block_scale(am, sd.m6, sd.fast6);
         S_out = S;
-        return encode_with_scale<MODE == MODE_SR>(y, S, g, rnd);
+        return encode_with_scale<MODE == MODE_SR>(y, S, T, rnd);
     }
 }
 

@@ -31,6 +31,31 @@ __device__ __forceinline__ void load_block_row(const float *p, f2 (&v)[8]) {
     }
 }
 
+// The raw bytes of one 1x16 block (32 B of bf16 or 64 B of fp32), loaded with
+// 128-bit reads so that the loads can be issued ahead of their use.
+template <typename T>
+struct RawBlock {
+    uint4 w[sizeof(T)];  // 16 elements * sizeof(T) bytes / 16 bytes per uint4
+};
+
+template <typename T>
+__device__ __forceinline__ void load_raw(const T *p, RawBlock<T> &b) {
+#pragma unroll
+    for (int k = 0; k < (int)sizeof(T); k++) b.w[k] = ld_nc(p + k * (16 / sizeof(T)));
+}
+
+__device__ __forceinline__ void unpack(const RawBlock<bf16_t> &b, f2 (&v)[8]) {
+    v[0] = bf16_pair(b.w[0].x); v[1] = bf16_pair(b.w[0].y); v[2] = bf16_pair(b.w[0].z); v[3] = bf16_pair(b.w[0].w);
+    v[4] = bf16_pair(b.w[1].x); v[5] = bf16_pair(b.w[1].y); v[6] = bf16_pair(b.w[1].z); v[7] = bf16_pair(b.w[1].w);
+}
+__device__ __forceinline__ void unpack(const RawBlock<float> &b, f2 (&v)[8]) {
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        v[2 * k] = f2{__uint_as_float(b.w[k].x), __uint_as_float(b.w[k].y)};
+        v[2 * k + 1] = f2{__uint_as_float(b.w[k].z), __uint_as_float(b.w[k].w)};
+    }
+}
+
 // A 16-byte chunk of one row: 8 bf16 or 4 fp32 elements.  When fewer than a
 // full chunk of columns remain, the missing elements read as zero.
 template <typename T>

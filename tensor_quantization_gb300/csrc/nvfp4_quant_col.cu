@@ -26,13 +26,17 @@ __device__ __forceinline__ void load_strip(const T *x, int64_t ld, int64_t r0, i
 template <int MODE, bool RHT, typename T>
 __global__ void __launch_bounds__(256) k_quant_col(const QArgs a) {
     constexpr int CW = Chunk<T>::W;
+    __shared__ DivTable tab;
     const uint32_t C = (uint32_t)a.cols;
     const uint32_t RB = (uint32_t)(a.rows >> 4);  // blocks per X^T row
     const uint32_t NCH = (C + CW - 1) / CW;
     const uint32_t n = RB * NCH;
     const int64_t csp = (RB + 3) & ~3u;
     const float g = global_scale_of(a.amax[0]);
+    build_table(tab, g, threadIdx.x, blockDim.x);
+    const ScaleDiv sd = make_scale_div(g);
     if (blockIdx.x == 0 && threadIdx.x == 0) a.gscale[0] = g;
+    __syncthreads();
     const T *x = static_cast<const T *>(a.x);
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const uint32_t ch = i % NCH, rb = i / NCH;
@@ -50,25 +54,25 @@ __global__ void __launch_bounds__(256) k_quant_col(const QArgs a) {
             uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
             if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, blk);
             uint32_t S;
-            const uint2 c = encode_block<MODE>(v, g, rnd, S);
+            const uint2 c = encode_block<MODE>(v, sd, tab, rnd, S);
             *reinterpret_cast<uint2 *>(a.codes_col + (int64_t)o * (a.rows >> 1) + 8 * rb) = c;
             a.scales_col[a.swizzled ? swizzle_offset(o, rb, csp) : (int64_t)blk] = (uint8_t)S;
         }
     }
 }
 
-// Codes of NP pairs against scale S (RNE): NP = 4 -> one word, NP = 2 -> low
-// half of a word.
+// Codes of NP pairs against divisor entry S (RNE): NP = 4 -> one word, NP = 2
+// -> low half of a word.
 template <int NP>
-__device__ __forceinline__ uint32_t encode_pairs_rne(const f2 (&y)[NP], uint32_t S, float g) {
-    const float Sf = e4m3_value(S);
-    if (Sf == 0.0f) return 0u;
-    const float d = __fmul_rn(Sf, g);
-    const Recip R = make_recip(d);
+__device__ __forceinline__ uint32_t encode_pairs_rne(const f2 (&y)[NP], uint32_t S, const DivTable &T) {
+    if (S == 0u) return 0u;
+    const Divisor &D = T.e[S & 0x7Fu];
     f2 q[4] = {f2{0.f, 0.f}, f2{0.f, 0.f}, f2{0.f, 0.f}, f2{0.f, 0.f}};
+    const bool fast = divisor_fast(D.d);
 #pragma unroll
-    for (int k = 0; k < NP; k++) q[k] = R.fast ? div2_fast(y[k], R) : f2{div_slow(y[k].x, d), div_slow(y[k].y, d)};
-    return e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y);
+    for (int k = 0; k < NP; k++)
+        q[k] = fast ? neg_quot2(y[k], D) : f2{neg_quot_slow(y[k].x, D.d), neg_quot_slow(y[k].y, D.d)};
+    return e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y) ^ 0x88888888u;
 }
 
 // 16x16 tiles: the 16/CW lanes that share a tile combine their maxima, then
@@ -82,8 +86,12 @@ __global__ void __launch_bounds__(256) k_quant_2d(const QArgs a) {
     const uint32_t NCH = C / CW;
     const uint32_t n = RB * NCH;  // a multiple of LPT
     const int64_t csp_row = (CB + 3) & ~3u, csp_col = (RB + 3) & ~3u;
+    __shared__ DivTable tab;
     const float g = global_scale_of(a.amax[0]);
+    build_table(tab, g, threadIdx.x, blockDim.x);
+    const ScaleDiv sd = make_scale_div(g);
     if (blockIdx.x == 0 && threadIdx.x == 0) a.gscale[0] = g;
+    __syncthreads();
     const T *x = static_cast<const T *>(a.x);
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t stride = gridDim.x * blockDim.x;
@@ -104,7 +112,7 @@ __global__ void __launch_bounds__(256) k_quant_2d(const QArgs a) {
 #pragma unroll
         for (int off = 1; off < LPT; off <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
         if (!active) continue;
-        const uint32_t S = block_scale(m, 6.0f, g);
+        const uint32_t S = block_scale(__uint_as_float(m), sd.m6, sd.fast6);
         const uint32_t cb = c0 >> 4;  // tile column
         if (a.want_row) {
 #pragma unroll
@@ -113,7 +121,7 @@ __global__ void __launch_bounds__(256) k_quant_2d(const QArgs a) {
                 f2 y[CW / 2];
 #pragma unroll
                 for (int p = 0; p < CW / 2; p++) y[p] = f2{rows[k].get(2 * p), rows[k].get(2 * p + 1)};
-                const uint32_t w = encode_pairs_rne<CW / 2>(y, S, g);
+                const uint32_t w = encode_pairs_rne<CW / 2>(y, S, tab);
                 uint8_t *dst = a.codes_row + r * (C >> 1) + (c0 >> 1);
                 if (CW == 8) *reinterpret_cast<uint32_t *>(dst) = w;
                 else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
@@ -128,7 +136,7 @@ __global__ void __launch_bounds__(256) k_quant_2d(const QArgs a) {
                 f2 v[8];
                 strip_column(rows, cc, v);
                 const uint4 none = make_uint4(0u, 0u, 0u, 0u);
-                const uint2 c = encode_with_scale<false>(v, S, g, none);
+                const uint2 c = encode_with_scale<false>(v, S, tab, none);
                 *reinterpret_cast<uint2 *>(a.codes_col + o * (a.rows >> 1) + 8 * rb) = c;
                 a.scales_col[a.swizzled ? swizzle_offset(o, rb, csp_col) : o * RB + rb] = (uint8_t)S;
             }

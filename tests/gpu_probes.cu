@@ -26,7 +26,7 @@ __global__ void k_e2m1_order(uint32_t *out) {
 __global__ void k_sr(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= n) return;
-    f2 v = sr_round2(f2{q[i], 0.f}, r[i], 0u);
+    f2 v = sr_round2(f2{q[i], 0.f}, r[i], 0u);  // symmetric: also used on -q
     out[i] = (uint8_t)(e2m1x8(v.x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 15u);
 }
 
@@ -48,11 +48,12 @@ __device__ __forceinline__ uint32_t mix(uint64_t x) {
     return (uint32_t)x;
 }
 
-// Exact division: the library's per-block path (fast when the reciprocal
-// range allows, IEEE otherwise) against __fdiv_rn.  Kinds: 0 random
-// significands, 1 near-midpoint quotients (y = RN(d*m), m a midpoint),
-// 2 random d over the whole fast range.  Quotients below 2^-11 only need to
-// stay below 2^-10 with the right sign.
+// Exact division: the library's per-block path (fast when the divisor range
+// allows, IEEE otherwise; both return -RN(y/d)) against __fdiv_rn.  Kinds:
+// 0 random significands, 1 near-midpoint quotients (y = RN(d*m), m a
+// midpoint), 2 random d over the whole fast range, 3 signed zeros.  Quotients
+// below 2^-11 only need to stay below 2^-10 with the right sign.  The scalar
+// block-scale quotient (positive numerators) is checked on the same pairs.
 __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *bad, float *first) {
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -73,21 +74,29 @@ __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *ba
         const double m = ((double)__uint_as_float((127u << 23) | (a & 0x7FFFFFu)) + 0x1p-24) *
                          (double)__uint_as_float((uint32_t)(115 + (mix(b) & 15u)) << 23);
         y = __double2float_rn((double)d * m);
+    } else if (kind == 3) {
+        y = 0.0f;
     } else {
         float q = __uint_as_float((127u << 23) | (a & 0x7FFFFFu)) * __uint_as_float((uint32_t)(112 + (b >> 28)) << 23);
         y = __fmul_rn(d, q);
     }
     if (a & 1u) y = -y;
-    const Recip R = make_recip(d);
-    f2 q = R.fast ? div2_fast(f2{y, y}, R) : f2{div_slow(y, d), div_slow(y, d)};
+    const Divisor D = make_divisor(d);
+    const bool fast = divisor_fast(d);
+    const f2 nq = fast ? neg_quot2(f2{y, y}, D) : f2{neg_quot_slow(y, d), neg_quot_slow(y, d)};
     const float ref = __fdiv_rn(y, d);
+    const float want = -(fast ? ref : fminf(fmaxf(ref, -8.f), 8.f));
     bool ok;
-    if (fabsf(ref) < 0x1p-11f) ok = fabsf(q.x) < 0x1p-10f && signbit(q.x) == signbit(ref);
-    else ok = __float_as_uint(q.x) == __float_as_uint(fminf(fmaxf(ref, -8.f), 8.f)) || fabsf(ref) >= 8.f;
-    ok = ok && __float_as_uint(q.x) == __float_as_uint(q.y);
+    if (fabsf(ref) < 0x1p-11f && ref != 0.0f) ok = fabsf(nq.x) < 0x1p-10f && signbit(nq.x) != signbit(ref);
+    else ok = __float_as_uint(nq.x) == __float_as_uint(want);
+    ok = ok && __float_as_uint(nq.x) == __float_as_uint(nq.y);
+    if (fast && fabsf(ref) >= 0x1p-11f && isfinite(ref)) {
+        const float ay = fabsf(y);
+        ok = ok && __float_as_uint(quot_pos(ay, D)) == __float_as_uint(__fdiv_rn(ay, d));
+    }
     if (!ok) {
         unsigned long long k = atomicAdd(bad, 1ull);
-        if (k < 4) { first[3 * k] = y; first[3 * k + 1] = d; first[3 * k + 2] = q.x; }
+        if (k < 4) { first[3 * k] = y; first[3 * k + 1] = d; first[3 * k + 2] = nq.x; }
     }
 }
 
