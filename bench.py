@@ -169,7 +169,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     dev = torch.device("cuda", local)
     build.build()
     nvfp4.load()
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
     x_cpu, mask = wl.make_input(w)
     x = x_cpu.to(dev)
     R, C = w.rows, w.cols
@@ -297,6 +297,14 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     return res
 
 
+def workload_of(args) -> wl.Workload:
+    w = wl.WORKLOADS[args.workload]
+    if args.shape:
+        r, c = (int(v) for v in args.shape.lower().split("x"))
+        w = w.resized(r, c)
+    return w
+
+
 def pad_launch_needed(w: wl.Workload) -> bool:
     if not w.swizzled:
         return False
@@ -369,6 +377,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=wl.HEADLINE, choices=list(wl.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (0 = skip)")
+    ap.add_argument("--shape", default=None, help="ROWSxCOLS override of the workload's shape (profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -383,7 +392,7 @@ def main():
     res = run_ours(args, rank, world)
     if rank == 0:
         if args.cpu_seconds > 0:
-            w = wl.WORKLOADS[args.workload]
+            w = workload_of(args)
             x_cpu, mask = wl.make_input(w)
             res["cpu_baseline"] = cpu_baseline(w, x_cpu, mask, args.cpu_seconds)
         print(json.dumps(res), flush=True)
