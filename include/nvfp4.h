@@ -144,6 +144,29 @@ nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16
                                    uint64_t seed, uint64_t offset, nvfp4_output *out,
                                    void *workspace, void *stream);
 
+/* nvfp4_quantize_rht_sr without a workspace argument.  The pages have no
+ * counterpart: this entry point exists for callers that cannot call cudaMalloc,
+ * for instance a serving runtime that reserves its whole device-memory budget
+ * at start-up and forbids allocation afterwards, or code that must not trigger
+ * the implicit device synchronisation an allocation can cause.  It allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine): the amax
+ * pass's scratch lives in a 256-byte device array inside the library, which
+ * every GPU that loads the library keeps until the process exits.  The pass
+ * needs 12 of those bytes for any input size; the call returns
+ * NVFP4_ERR_UNSUPPORTED if the library's workspace need ever exceeds the array.
+ * Inputs and outputs are as for nvfp4_quantize_rht_sr, whose checks (sizes
+ * included) apply unchanged.
+ *
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture.  Every call then clears the scratch
+ * on the given stream (it is cleared even when the arguments are rejected; no
+ * caller buffer is touched in that case).  All calls share the one array:
+ * calls whose work overlaps on the GPU (other streams, other threads) race on
+ * it and must be serialised by the caller. */
+nvfp4_status nvfp4_quantize_rht_sr_static(const nvfp4_input *in, uint32_t flags, uint16_t sign_mask,
+                                          uint64_t seed, uint64_t offset, nvfp4_output *out, void *stream);
+
 /* Four-over-six (RNE candidates for M = 6 and M = 4).  1x16 blocks, per-tensor
  * or per-row global scale; per-row needs exactly one orientation (rowwise). */
 nvfp4_status nvfp4_quantize_four_over_six(const nvfp4_input *in, uint32_t flags, nvfp4_output *out,

@@ -44,7 +44,7 @@ class Output(ctypes.Structure):
 
 EXPORTS = ("nvfp4_workspace_bytes", "nvfp4_scale_bytes", "nvfp4_amax", "nvfp4_quantize_rne",
            "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr", "nvfp4_quantize_four_over_six",
-           "nvfp4_dequantize", "nvfp4_status_string")
+           "nvfp4_dequantize", "nvfp4_status_string", "nvfp4_quantize_rht_sr_static")
 
 
 def lib_path() -> str:
@@ -72,9 +72,10 @@ def load(path: str | None = None):
     L.nvfp4_quantize_sr.argtypes = [PI, u32, u64, u64, PO, vp, vp]
     L.nvfp4_quantize_rht_sr.argtypes = [PI, u32, ctypes.c_uint16, u64, u64, PO, vp, vp]
     L.nvfp4_quantize_four_over_six.argtypes = [PI, u32, PO, vp, vp]
+    L.nvfp4_quantize_rht_sr_static.argtypes = [PI, u32, ctypes.c_uint16, u64, u64, PO, vp]
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, u32, vp, i32, vp]
     for f in ("nvfp4_amax", "nvfp4_quantize_rne", "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr",
-              "nvfp4_quantize_four_over_six", "nvfp4_dequantize"):
+              "nvfp4_quantize_four_over_six", "nvfp4_dequantize", "nvfp4_quantize_rht_sr_static"):
         getattr(L, f).restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -153,6 +154,14 @@ def nvfp4_quantize_rht_sr(x, flags, sign_mask, seed, offset, out: Output, worksp
     _check(load().nvfp4_quantize_rht_sr(ctypes.byref(make_input(x)), flags, sign_mask & 0xFFFF, seed, offset,
                                         ctypes.byref(out), _ptr(workspace), _stream(stream)),
            "nvfp4_quantize_rht_sr")
+
+
+def nvfp4_quantize_rht_sr_static(x, flags, sign_mask, seed, offset, out: Output, stream=None) -> None:
+    """RHT + SR quantize with the amax scratch held inside the library (for
+    callers that cannot allocate device memory; see include/nvfp4.h)."""
+    _check(load().nvfp4_quantize_rht_sr_static(ctypes.byref(make_input(x)), flags, sign_mask & 0xFFFF, seed,
+                                               offset, ctypes.byref(out), _stream(stream)),
+           "nvfp4_quantize_rht_sr_static")
 
 
 def nvfp4_quantize_four_over_six(x, flags, out: Output, workspace, stream=None) -> None:
