@@ -242,5 +242,9 @@ __device__ __forceinline__ f2 rht_mult(uint32_t mask, int k) {
 __device__ __forceinline__ int64_t swizzle_offset(int64_t r, int64_t j, int64_t cs_p) {
     return ((r >> 7) * (cs_p >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (j & 3);
 }
+// The same in 32-bit arithmetic, for scale arrays below 4 GiB.
+__device__ __forceinline__ uint32_t swizzle_offset32(uint32_t r, uint32_t j, uint32_t cs_p) {
+    return ((r >> 7) * (cs_p >> 2) + (j >> 2)) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u + (j & 3u);
+}
 
 }  // namespace nvfp4

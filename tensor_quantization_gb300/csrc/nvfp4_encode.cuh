@@ -16,18 +16,24 @@ enum Mode { MODE_RNE = 0, MODE_SR = 1, MODE_4O6 = 2 };
 // Decode scale of the tensor / row: g = A / (6 * 448).
 __device__ __forceinline__ float global_scale_of(float A) { return __fdiv_rn(A, 2688.0f); }
 
-// max |v| over a block (NaN if any element is NaN).
+// max |v| over a block (NaN if any element is NaN): a tree of 3-input
+// max.NaN instructions (sm_100+), written as one asm block so that ptxas
+// folds every |.| into their operand modifiers.
 __device__ __forceinline__ float block_amax(const f2 (&v)[8]) {
-    float m0 = absmax_nan(v[0].x, v[0].y), m1 = absmax_nan(v[1].x, v[1].y);
-    float m2 = absmax_nan(v[2].x, v[2].y), m3 = absmax_nan(v[3].x, v[3].y);
-#pragma unroll
-    for (int k = 4; k < 8; k += 4) {
-        m0 = absmax_nan(m0, absmax_nan(v[k].x, v[k].y));
-        m1 = absmax_nan(m1, absmax_nan(v[k + 1].x, v[k + 1].y));
-        m2 = absmax_nan(m2, absmax_nan(v[k + 2].x, v[k + 2].y));
-        m3 = absmax_nan(m3, absmax_nan(v[k + 3].x, v[k + 3].y));
-    }
-    return absmax_nan(absmax_nan(m0, m1), absmax_nan(m2, m3));
+    float m;
+    asm("{\n\t.reg .f32 a<16>, b<6>, c<2>;\n\t"
+        "abs.f32 a0, %1; abs.f32 a1, %2; abs.f32 a2, %3; abs.f32 a3, %4;\n\t"
+        "abs.f32 a4, %5; abs.f32 a5, %6; abs.f32 a6, %7; abs.f32 a7, %8;\n\t"
+        "abs.f32 a8, %9; abs.f32 a9, %10; abs.f32 a10, %11; abs.f32 a11, %12;\n\t"
+        "abs.f32 a12, %13; abs.f32 a13, %14; abs.f32 a14, %15; abs.f32 a15, %16;\n\t"
+        "max.NaN.f32 b0, a0, a1, a2; max.NaN.f32 b1, a3, a4, a5; max.NaN.f32 b2, a6, a7, a8;\n\t"
+        "max.NaN.f32 b3, a9, a10, a11; max.NaN.f32 b4, a12, a13, a14;\n\t"
+        "max.NaN.f32 c0, b0, b1, b2; max.NaN.f32 c1, b3, b4, a15;\n\t"
+        "max.NaN.f32 %0, c0, c1;\n\t}"
+        : "=f"(m)
+        : "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y), "f"(v[3].x), "f"(v[3].y),
+          "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x), "f"(v[6].y), "f"(v[7].x), "f"(v[7].y));
+    return m;
 }
 
 // The 128 element divisors of one global scale.  Entry s holds
@@ -146,11 +152,21 @@ __device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &
     }
 }
 
+// The 16 RHT output multipliers (+-0.25 by the sign mask), prepared once per
+// CTA in shared memory and read back as 4 x 128-bit per block.
+struct RhtMult {
+    f2 m[8];
+};
+
+__device__ __forceinline__ void build_rht_mult(RhtMult &M, uint32_t sign_mask, int tid) {
+    if (tid < 8) M.m[tid] = rht_mult(sign_mask, tid);
+}
+
 // RHT of a block in place: butterfly, then * (+-0.25).
-__device__ __forceinline__ void rht16(f2 (&v)[8], uint32_t sign_mask) {
+__device__ __forceinline__ void rht16(f2 (&v)[8], const RhtMult &M) {
     fwht16(v);
 #pragma unroll
-    for (int k = 0; k < 8; k++) v[k] = mul2(v[k], rht_mult(sign_mask, k));
+    for (int k = 0; k < 8; k++) v[k] = mul2(v[k], M.m[k]);
 }
 
 }  // namespace nvfp4

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
@@ -25,6 +26,11 @@ struct QArgs {
 
 // Device properties, cached per device.
 int sm_count();
+
+// 2-D tensor map over X (row pitch ld elements) with a box of box_cols x
+// box_rows elements, 128-byte swizzle, zero fill outside the tensor.
+bool make_tmap_2d(CUtensorMap *map, const void *x, int elem_bytes, int64_t rows, int64_t cols, int64_t ld,
+                  uint32_t box_cols, uint32_t box_rows);
 
 // ---- launchers (return cudaGetLastError() after the launch) ----
 // Per-tensor amax (optionally of RHT blocks along rows (col=0) or columns

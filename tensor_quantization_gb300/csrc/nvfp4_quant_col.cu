@@ -27,6 +27,8 @@ template <int MODE, bool RHT, typename T>
 __global__ void __launch_bounds__(256) k_quant_col(const QArgs a) {
     constexpr int CW = Chunk<T>::W;
     __shared__ DivTable tab;
+    __shared__ RhtMult rm;
+    if (RHT) build_rht_mult(rm, a.sign_mask, threadIdx.x);
     const uint32_t C = (uint32_t)a.cols;
     const uint32_t RB = (uint32_t)(a.rows >> 4);  // blocks per X^T row
     const uint32_t NCH = (C + CW - 1) / CW;
@@ -49,7 +51,7 @@ __global__ void __launch_bounds__(256) k_quant_col(const QArgs a) {
             if (o >= C) break;
             f2 v[8];
             strip_column(rows, cc, v);
-            if (RHT) rht16(v, a.sign_mask);
+            if (RHT) rht16(v, rm);
             const uint64_t blk = (uint64_t)o * RB + rb;
             uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
             if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, blk);

@@ -11,82 +11,195 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tma.cuh"
 
 namespace nvfp4 {
 
 // Scale bytes of 4 consecutive blocks of a row go out as one 32-bit store
 // (lanes 4m..4m+3 hold blocks j..j+3 with j % 4 == 0); otherwise one byte.
-__device__ __forceinline__ void store_scale(const QArgs &a, uint8_t *scales, uint32_t S, int64_t r, uint32_t j,
-                                            uint32_t CS, int64_t csp, bool active, bool words) {
+// Scale arrays stay below 4 GiB, so offsets are 32-bit.
+__device__ __forceinline__ void store_scale(const QArgs &a, uint8_t *scales, uint32_t S, uint32_t r, uint32_t j,
+                                            uint32_t CS, uint32_t csp, bool active, bool words) {
     if (words) {
         const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, S, 1);
         const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, S, 2);
         const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, S, 3);
         if (active && (j & 3u) == 0) {
-            const int64_t off = a.swizzled ? swizzle_offset(r, j, csp) : r * CS + j;
+            const uint32_t off = a.swizzled ? swizzle_offset32(r, j, csp) : r * CS + j;
             *reinterpret_cast<uint32_t *>(scales + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
         }
     } else if (active) {
-        scales[a.swizzled ? swizzle_offset(r, j, csp) : r * CS + j] = (uint8_t)S;
+        scales[a.swizzled ? swizzle_offset32(r, j, csp) : r * CS + j] = (uint8_t)S;
     }
 }
 
+// Encode one block from its raw bytes (flat block index i, for the Philox
+// counter); returns the codes and writes S.
 template <int MODE, bool RHT, typename T>
-__global__ void __launch_bounds__(256) k_quant_row(const QArgs a) {
+__device__ __forceinline__ uint2 row_block(const QArgs &a, const ScaleDiv &sd, const DivTable &tab, const RhtMult &rm,
+                                           const RawBlock<T> &raw, uint32_t i, uint32_t &S) {
+    f2 v[8];
+    unpack(raw, v);
+    if (RHT) rht16(v, rm);
+    uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+    if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, i);
+    return encode_block<MODE>(v, sd, tab, rnd, S);
+}
+
+// ---------------------------------------------------------------------
+// Per-tensor rowwise quantize, input staged through shared memory by TMA.
+//
+// The input is cut into tiles of 64 rows x 64 columns (4 blocks per row).
+// One thread owns one tile row, i.e. 4 consecutive blocks: its codes are 32
+// contiguous bytes and its scales one 32-bit word.  Persistent CTAs walk the
+// tiles round-robin; thread 0 keeps kStages tiles in flight with TMA copies
+// into 128-byte-swizzled buffers, so the 16-byte chunks a warp reads sit in
+// distinct bank groups.  Boxes outside the tensor are zero-filled, which also
+// yields the zero pad bytes of the swizzled scale layout.
+constexpr int kTileRows = 64;
+constexpr int kTileCols = 64;
+constexpr int kStages = 1;
+
+template <typename T>
+struct RowTile {
+    static constexpr int kBoxCols = 128 / (int)sizeof(T);  // one 128-byte swizzle span
+    static constexpr int kBoxes = kTileCols / kBoxCols;    // 1 (bf16) or 2 (fp32)
+    static constexpr int kBoxBytes = kTileRows * 128;
+    static constexpr int kStageBytes = kBoxes * kBoxBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+};
+
+// Raw bytes of block b (0..3) of tile row `row`: chunk c of a 128-byte box
+// row is stored at chunk position c ^ (row % 8).
+template <typename T>
+__device__ __forceinline__ void stage_block(const uint8_t *stage, int row, int b, RawBlock<T> &raw) {
+    constexpr int kChunks = (int)sizeof(T);  // 16-byte chunks per block
+    constexpr int kPerBoxRow = 8 / kChunks;  // blocks per box row
+    const uint8_t *base = stage + (b / kPerBoxRow) * RowTile<T>::kBoxBytes + row * 128;
+#pragma unroll
+    for (int k = 0; k < kChunks; k++) {
+        const int c = (b % kPerBoxRow) * kChunks + k;
+        raw.w[k] = *reinterpret_cast<const uint4 *>(base + ((c ^ (row & 7)) << 4));
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void issue_tile(const CUtensorMap *map, uint8_t *stage, uint64_t *bar, uint32_t tr,
+                                           uint32_t tc) {
+    mbar_arrive_expect_tx(bar, RowTile<T>::kStageBytes);
+#pragma unroll
+    for (int b = 0; b < RowTile<T>::kBoxes; b++)
+        tma_load_2d(stage + b * RowTile<T>::kBoxBytes, map, (int32_t)(tc * kTileCols + b * RowTile<T>::kBoxCols),
+                    (int32_t)(tr * kTileRows), bar);
+}
+
+template <int MODE, bool RHT, typename T>
+__global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
+    extern __shared__ uint8_t dyn_smem[];
     __shared__ DivTable tab;
-    const uint32_t CS = (uint32_t)(a.cols >> 4);
-    const uint32_t n = (uint32_t)a.rows * CS;
-    const int64_t csp = (CS + 3) & ~3u;
+    __shared__ RhtMult rm;
+    __shared__ __align__(8) uint64_t full[kStages];
+    uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
+    const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, CS = C >> 4, csp = (CS + 3) & ~3u;
+    const uint32_t Rp = (R + 127) & ~127u;
+    const uint32_t ntc = (C + kTileCols - 1) / kTileCols, ntr = (R + kTileRows - 1) / kTileRows;
+    const uint32_t ntiles = ntc * ntr;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; s++) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int k = 0; k < kStages; k++) {
+            const uint32_t t = blockIdx.x + k * gridDim.x;
+            if (t < ntiles) issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], t / ntc, t % ntc);
+        }
+    }
+    // per-scale state, built while the first copies are in flight
     const float g = global_scale_of(a.amax[0]);
-    build_table(tab, g, threadIdx.x, blockDim.x);
+    build_table(tab, g, tid, blockDim.x);
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
     const ScaleDiv sd = make_scale_div(g);
-    if (blockIdx.x == 0 && threadIdx.x == 0) a.gscale[0] = g;
+    if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
     __syncthreads();
 
-    // this CTA's range of blocks: a multiple of 32 long, so warps stay whole
-    const uint32_t per = ((n + gridDim.x - 1) / gridDim.x + 31) & ~31u;
-    const uint32_t b0 = blockIdx.x * per;
-    if (b0 >= n) return;
-    const uint32_t b1 = min(n, b0 + per);
-    const bool words = (CS & 3u) == 0;
-    const T *x = static_cast<const T *>(a.x);
-
-    uint32_t i = b0 + threadIdx.x;
-    uint32_t r = i / CS, j = i - r * CS;
-    const uint32_t dr = blockDim.x / CS, dj = blockDim.x % CS;
-    RawBlock<T> cur, nxt;
-    if (i < b1) load_raw(x + (int64_t)r * a.ld + 16 * j, cur);
-    for (uint32_t base = b0 + (threadIdx.x & ~31u); base < b1; base += blockDim.x) {
-        const bool active = i < b1;
-        // next block of this thread
-        const uint32_t i2 = i + blockDim.x;
-        uint32_t r2 = r + dr, j2 = j + dj;
-        if (j2 >= CS) { j2 -= CS; ++r2; }
-        if (i2 < b1) load_raw(x + (int64_t)r2 * a.ld + 16 * j2, nxt);
-        uint32_t S = 0;
-        if (active) {
-            f2 v[8];
-            unpack(cur, v);
-            if (RHT) rht16(v, a.sign_mask);
-            uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
-            if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, i);
-            const uint2 c = encode_block<MODE>(v, sd, tab, rnd, S);
-            *reinterpret_cast<uint2 *>(a.codes_row + (int64_t)r * (a.cols >> 1) + 8 * j) = c;
+    // vector stores only where every address is aligned for them
+    const bool codes16 = (C & 31u) == 0 && (reinterpret_cast<uintptr_t>(a.codes_row) & 15u) == 0;
+    const bool words = (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
+    const bool lin_words = words && (CS & 3u) == 0;
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t t = blockIdx.x + k * gridDim.x;
+        if (t >= ntiles) break;
+        const uint32_t s = k % kStages;
+        if (!mbar_wait(&full[s], (k / kStages) & 1u)) {  // a copy never landed: bounded, visible failure
+            atomicAdd(&g_wait_timeouts, 1u);
+            a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
         }
-        store_scale(a, a.scales_row, S, r, j, CS, csp, active, words);
-        i = i2;
-        r = r2;
-        j = j2;
-        cur = nxt;
+        const uint32_t tr = t / ntc, tc = t - tr * ntc;
+        const uint32_t row = tr * kTileRows + tid, j0 = tc * 4;
+        const uint8_t *stage = stages + s * RowTile<T>::kStageBytes;
+        if (row < R) {
+            uint32_t S[4] = {0u, 0u, 0u, 0u};
+            uint2 c[4];
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                if (j0 + b < CS) {
+                    RawBlock<T> raw;
+                    stage_block<T>(stage, tid, b, raw);
+                    c[b] = row_block<MODE, RHT, T>(a, sd, tab, rm, raw, row * CS + j0 + b, S[b]);
+                }
+            }
+            uint8_t *codes = a.codes_row + (int64_t)row * (C >> 1) + j0 * 8;
+            if (codes16 && j0 + 3 < CS) {
+                reinterpret_cast<uint4 *>(codes)[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+                reinterpret_cast<uint4 *>(codes)[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++)
+                    if (j0 + b < CS) reinterpret_cast<uint2 *>(codes)[b] = c[b];
+            }
+            const uint32_t word = S[0] | (S[1] << 8) | (S[2] << 16) | (S[3] << 24);
+            if (a.swizzled) {
+                uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+                if (words) {
+                    *reinterpret_cast<uint32_t *>(dst) = word;
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 4; b++) dst[b] = (uint8_t)S[b];
+                }
+            } else if (lin_words && j0 + 3 < CS) {
+                *reinterpret_cast<uint32_t *>(a.scales_row + row * CS + j0) = word;
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++)
+                    if (j0 + b < CS) a.scales_row[row * CS + j0 + b] = (uint8_t)S[b];
+            }
+        } else if (a.swizzled && row < Rp) {  // pad rows of the swizzled layout
+            uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+            if (words) {
+                *reinterpret_cast<uint32_t *>(dst) = 0u;
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++) dst[b] = 0;
+            }
+        }
+        __syncthreads();  // every thread is done with stage s
+        if (tid == 0) {
+            const uint32_t tn = t + kStages * gridDim.x;
+            if (tn < ntiles) {
+                fence_async_shared();
+                issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], tn / ntc, tn % ntc);
+            }
+        }
     }
 }
 
 template <int MODE, bool RHT, typename T>
 __global__ void __launch_bounds__(256) k_quant_rowscaled(const QArgs a) {
     __shared__ DivTable tab;
+    __shared__ RhtMult rm;
     __shared__ uint32_t red[32];
     const uint32_t CS = (uint32_t)(a.cols >> 4);
-    const int64_t csp = (CS + 3) & ~3u;
+    const uint32_t csp = (CS + 3) & ~3u;
+    if (RHT) build_rht_mult(rm, a.sign_mask, threadIdx.x);
     const bool words = (CS & 3u) == 0;
     const T *x = static_cast<const T *>(a.x);
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
@@ -122,13 +235,13 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled(const QArgs a) {
                 load_raw(xr + 16 * j, b);
                 f2 v[8];
                 unpack(b, v);
-                if (RHT) rht16(v, a.sign_mask);
+                if (RHT) rht16(v, rm);
                 uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
                 if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, (uint64_t)r * CS + j);
                 const uint2 c = encode_block<MODE>(v, sd, tab, rnd, S);
                 *reinterpret_cast<uint2 *>(a.codes_row + r * (a.cols >> 1) + 8 * j) = c;
             }
-            store_scale(a, a.scales_row, S, r, j, CS, csp, active, words);
+            store_scale(a, a.scales_row, S, (uint32_t)r, j, CS, csp, active, words);
         }
         __syncthreads();  // the next row rebuilds the table
     }
@@ -147,8 +260,23 @@ static int grid_for(K kernel, int threads, int64_t work_items) {
 template <int MODE, bool RHT, typename T>
 static cudaError_t run_row(const QArgs &a, cudaStream_t s) {
     auto k = k_quant_row<MODE, RHT, T>;
-    const int grid = grid_for(k, 256, (a.cols >> 4) * a.rows);
-    k<<<grid, 256, 0, s>>>(a);
+    constexpr int smem = RowTile<T>::kSmemBytes;
+    static bool configured = false;  // one attribute call per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    CUtensorMap map;
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, RowTile<T>::kBoxCols, kTileRows))
+        return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTileRows, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t tiles = ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    k<<<grid, kTileRows, smem, s>>>(map, a);
     return cudaGetLastError();
 }
 
