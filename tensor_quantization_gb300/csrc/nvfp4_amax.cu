@@ -55,35 +55,38 @@ __global__ void __launch_bounds__(256) k_amax_plain(const QArgs a) {
     publish_tensor_amax(a, m, false);
 }
 
-// RHT blocks along rows.  Each CTA scans one contiguous range of blocks with
-// the next block's loads in flight while the current one is transformed.
+// RHT blocks along rows.  Each CTA scans one contiguous range of blocks; a
+// thread keeps kAmaxDepth blocks' loads in flight (consecutive blocks of its
+// range, 32 bytes each for bf16) and transforms them as they land.
+constexpr int kAmaxDepth = 1;
+
 template <typename T>
 __global__ void __launch_bounds__(256) k_amax_rht_row(const QArgs a) {
     const uint32_t CS = (uint32_t)(a.cols >> 4);
     const uint32_t n = (uint32_t)a.rows * CS;
-    const uint32_t per = ((n + gridDim.x - 1) / gridDim.x + 31) & ~31u;
+    const uint32_t span = blockDim.x * kAmaxDepth;  // blocks per CTA step
+    const uint32_t per = ((n + gridDim.x - 1) / gridDim.x + span - 1) / span * span;
     const uint32_t b0 = blockIdx.x * per, b1 = min(n, b0 + per);
     const T *x = static_cast<const T *>(a.x);
     uint32_t m = 0;
-    if (b0 < n) {
-        uint32_t i = b0 + threadIdx.x;
-        uint32_t r = i / CS, j = i - r * CS;
-        const uint32_t dr = blockDim.x / CS, dj = blockDim.x % CS;
-        RawBlock<T> cur, nxt;
-        if (i < b1) load_raw(x + (int64_t)r * a.ld + 16 * j, cur);
-        while (i < b1) {
-            uint32_t r2 = r + dr, j2 = j + dj;
-            if (j2 >= CS) { j2 -= CS; ++r2; }
-            const uint32_t i2 = i + blockDim.x;
-            if (i2 < b1) load_raw(x + (int64_t)r2 * a.ld + 16 * j2, nxt);
-            f2 v[8];
-            unpack(cur, v);
-            fwht16(v);
-            m = max(m, __float_as_uint(block_amax(v)));
-            i = i2;
-            r = r2;
-            j = j2;
-            cur = nxt;
+    for (uint32_t base = b0; base < b1; base += span) {
+        RawBlock<T> raw[kAmaxDepth];
+#pragma unroll
+        for (int k = 0; k < kAmaxDepth; k++) {
+            const uint32_t i = base + k * blockDim.x + threadIdx.x;
+            if (i < b1) {
+                const uint32_t r = i / CS, j = i - r * CS;
+                load_raw(x + (int64_t)r * a.ld + 16 * j, raw[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAmaxDepth; k++) {
+            if (base + k * blockDim.x + threadIdx.x < b1) {
+                f2 v[8];
+                unpack(raw[k], v);
+                fwht16(v);
+                m = max(m, __float_as_uint(block_amax(v)));
+            }
         }
     }
     publish_tensor_amax(a, m, true);

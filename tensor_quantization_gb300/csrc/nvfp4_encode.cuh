@@ -152,6 +152,82 @@ __device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &
     }
 }
 
+// ---------------------------------------------------------------- fast path
+// When every divisor of a global scale g is in the fast division range (true
+// unless the tensor's amax is extreme, NaN or infinite), blocks skip the
+// per-block range test.  With S != 0x7F guaranteed (the block amax is finite),
+// an all-zero block is the only special case and is masked to +0 codes.
+__device__ __forceinline__ bool scale_all_fast(float g) {
+    // smallest divisor 2^-9 * g, largest 448 * g (x4 for the folded RHT)
+    return g >= 0x1p-71f && g <= 0x1p89f;  // false for NaN
+}
+
+// The RHT's outputs are y_j = s_j * 0.25 * v'_j (v' = butterfly output).  On
+// the fast path the 0.25 goes into the divisor (y/d = v'/(4d) exactly: a
+// quotient that could differ, from a v' so small that 0.25 * v' rounds, is
+// below 2^-40 and keeps its sign, so its code cannot change) and the signs s_j
+// into the code-sign flip.  `signs` holds bit 4e+3 for every negated element
+// e of the 8 in one code word.
+template <bool SR>
+__device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32_t S, bool fold4,
+                                             uint2 signs, const uint4 &rnd) {
+    if (fold4) {
+        D.d = __fmul_rn(D.d, 4.0f);
+        D.nrh = __fmul_rn(D.nrh, 0.25f);
+        D.nrd = __fmul_rn(D.nrd, 0.25f);
+        D.nrl = __fmul_rn(D.nrl, 0.25f);
+    }
+    f2 nq[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) nq[k] = neg_quot2(v[k], D);
+    if (SR) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], rbyte(rnd, 2 * k), rbyte(rnd, 2 * k + 1));
+    }
+    const uint32_t keep = S ? 0xFFFFFFFFu : 0u;
+    uint2 c;
+    c.x = (e2m1x8(nq[0].x, nq[0].y, nq[1].x, nq[1].y, nq[2].x, nq[2].y, nq[3].x, nq[3].y) ^ 0x88888888u ^ signs.x) & keep;
+    c.y = (e2m1x8(nq[4].x, nq[4].y, nq[5].x, nq[5].y, nq[6].x, nq[6].y, nq[7].x, nq[7].y) ^ 0x88888888u ^ signs.y) & keep;
+    return c;
+}
+
+// One block on the fast path.  v holds the raw block (RHT: the butterfly is
+// applied here and the 0.25 / signs are folded as above).
+template <int MODE, bool RHT>
+__device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &sd, const DivTable &T,
+                                                   uint2 signs, const uint4 &rnd, uint32_t &S_out) {
+    if (RHT) fwht16(v);
+    float am = block_amax(v);
+    if (RHT) am = __fmul_rn(am, 0.25f);  // = max |y|: rounding is monotone
+    if (MODE == MODE_4O6) {
+        const uint32_t S6 = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m6));
+        const uint32_t S4 = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m4));
+        const Divisor D6 = T.e[S6], D4 = T.e[S4];
+        const uint2 c6 = encode_fast<false>(v, D6, S6, false, signs, rnd);
+        const uint2 c4 = encode_fast<false>(v, D4, S4, false, signs, rnd);
+        const float e6 = candidate_error(v, c6, S6 ? D6.d : 0.0f);
+        const float e4 = candidate_error(v, c4, S4 ? D4.d : 0.0f);
+        const bool pick4 = e4 < e6;  // ties keep map-to-6
+        S_out = pick4 ? S4 : S6;
+        return pick4 ? c4 : c6;
+    } else {
+        const uint32_t S = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m6));
+        S_out = S;
+        return encode_fast<MODE == MODE_SR>(v, T.e[S], S, RHT, signs, rnd);
+    }
+}
+
+// Code-word sign flips for the RHT sign mask: bit 4e+3 for negated element e.
+__device__ __forceinline__ uint2 rht_sign_words(uint32_t mask) {
+    uint2 w = make_uint2(0u, 0u);
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        w.x |= ((mask >> e) & 1u) << (4 * e + 3);
+        w.y |= ((mask >> (8 + e)) & 1u) << (4 * e + 3);
+    }
+    return w;
+}
+
 // The 16 RHT output multipliers (+-0.25 by the sign mask), prepared once per
 // CTA in shared memory and read back as 4 x 128-bit per block.
 struct RhtMult {

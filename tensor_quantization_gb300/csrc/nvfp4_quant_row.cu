@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
     build_table(tab, g, tid, blockDim.x);
     if (RHT) build_rht_mult(rm, a.sign_mask, tid);
     const ScaleDiv sd = make_scale_div(g);
+    const bool fast = scale_all_fast(g);  // uniform: every divisor in the fast range
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
     if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
     __syncthreads();
 
@@ -139,12 +141,27 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
         if (row < R) {
             uint32_t S[4] = {0u, 0u, 0u, 0u};
             uint2 c[4];
+            if (fast) {
 #pragma unroll
-            for (int b = 0; b < 4; b++) {
-                if (j0 + b < CS) {
-                    RawBlock<T> raw;
-                    stage_block<T>(stage, tid, b, raw);
-                    c[b] = row_block<MODE, RHT, T>(a, sd, tab, rm, raw, row * CS + j0 + b, S[b]);
+                for (int b = 0; b < 4; b++) {
+                    if (j0 + b < CS) {
+                        RawBlock<T> raw;
+                        stage_block<T>(stage, tid, b, raw);
+                        f2 v[8];
+                        unpack(raw, v);
+                        uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+                        if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, row * CS + j0 + b);
+                        c[b] = encode_block_fast<MODE, RHT>(v, sd, tab, signs, rnd, S[b]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    if (j0 + b < CS) {
+                        RawBlock<T> raw;
+                        stage_block<T>(stage, tid, b, raw);
+                        c[b] = row_block<MODE, RHT, T>(a, sd, tab, rm, raw, row * CS + j0 + b, S[b]);
+                    }
                 }
             }
             uint8_t *codes = a.codes_row + (int64_t)row * (C >> 1) + j0 * 8;
