@@ -74,6 +74,14 @@ def counted_bytes(w: wl.Workload, elem: int = 2) -> dict:
 
 
 # ---------------------------------------------------------------- peaks
+def clk_max_mhz() -> float:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        return 2070.0
+
+
 def hbm_peak() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -83,18 +91,23 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(kernel: str, workload: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary of this kernel on
-    this workload, if its recorded source digest matches the current sources."""
+def profile_field(kernel: str, workload: str, field: str) -> float | None:
+    """A number recorded in the committed ncu summary of this kernel on this
+    workload (profiles/<kernel>__<workload>.md), if the summary's source digest
+    matches the current kernel sources; None otherwise."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m = re.search(field + r":\s*([0-9.eE+]+)", text)
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     if not m or not s or s.group(1) != source_digest():
         return None
     return float(m.group(1))
+
+
+def profile_traffic(kernel: str, workload: str) -> float | None:
+    return profile_field(kernel, workload, "traffic_bytes_per_launch")
 
 
 def source_digest() -> str:
@@ -271,6 +284,29 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         unit_desc = "2 B read + 0.5 B codes + 1/16 B scale per element (+ scale words)"
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = profile_traffic(dom, w.name)
+    hbm_view = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": dom_bytes,
+                "per_unit": unit_desc, "ms_per_launch": round(dom_ms, 5)}
+    roofline = hbm_view
+    wipe = profile_field(dom, w.name, "warp_inst_per_element") if dom == "k_quant" else None
+    if wipe:
+        # the quantize kernel reads its input from L2 and is issue-bound: its
+        # roofline is the issue rate, 1 warp instruction per cycle per scheduler
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clk_max_mhz()
+        inst = wipe * R * C
+        peak_i = sms * 4 * mhz * 1e6 / 1e9
+        ach_i = inst / (dom_ms * 1e-3) / 1e9
+        roofline = {"bound": "alu", "kernel": dom, "achieved": round(ach_i, 1), "peak": round(peak_i, 1),
+                    "unit": "Gwarp-inst/s", "frac": round(ach_i / peak_i, 4), "traffic": traffic,
+                    "peak_source": f"{sms} SMs x 4 schedulers x 1 warp-instruction/cycle x {mhz:.0f} MHz max SM clock",
+                    "instructions_per_launch": round(inst),
+                    "instructions_source": "ncu smsp__inst_executed.sum per element, profiles/k_quant__"
+                                           + w.name + ".md",
+                    "ms_per_launch": round(dom_ms, 5), "hbm_view": {k: hbm_view[k] for k in
+                                                                     ("achieved", "peak", "unit", "frac")}}
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -281,11 +317,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
                    "parallelism": f"replicas{world}" if world > 1 else "single_gpu"},
         "counted_bytes_per_step": nbytes["total"],
         "pct_of_peak": round(100 * value / world / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                     else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": dom_bytes,
-                     "per_unit": unit_desc, "ms_per_launch": round(dom_ms, 5)},
+        "roofline": roofline,
         "kernels_ms": {"k_amax": round(k1, 5) if split else None, "k_quant": round(k2, 5)},
         "e2e": {"value": round(nbytes["total"] / (statistics.mean(e2e_ms) * 1e-3) / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
