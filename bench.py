@@ -173,6 +173,22 @@ class ClockSampler:
                 "source": "nvml" if self.ok else "unavailable"}
 
 
+# ------------------------------------------------------------ ranks
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's timed total: every rank's number, MAX-reduced."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank_step: int, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank processes its own batch (replicas),
+    all in the slowest rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------- our arm
 def run_ours(args, rank: int, world: int) -> dict | None:
     from tensor_quantization_gb300 import build, nvfp4
@@ -244,11 +260,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
     k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
 
     # end to end through the public API: pinned host input -> device, the
     # fused call (amax pass + encode), codes/scales/scale words -> pinned host
@@ -274,7 +286,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
 
     nbytes = counted_bytes(w)
     ms = total_ms / args.steps
-    value = world * nbytes["total"] / (ms * 1e-3) / 1e9
+    value = aggregate_gbs(nbytes["total"], ms, world)
     peak, peak_src = hbm_peak()
     k1, k2 = statistics.mean(k1_ms), statistics.mean(k2_ms)
     if split and k1 > k2:
