@@ -107,6 +107,10 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
     a.sign_mask = sign_mask;
     a.seed = seed;
     a.offset = offset;
+    for (int i = 0; i < 10; i++) {
+        a.round_key0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
+        a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+    }
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
     if (per_row) {
         st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, mode, rht, s));

@@ -203,6 +203,24 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
     return make_uint4(c0, c1, c2, c3);
 }
 
+// The same with the ten round keys given (k0[i] = seed lo + i * 0x9E3779B9,
+// k1[i] = seed hi + i * 0xBB67AE85).
+__device__ __forceinline__ uint4 philox4x32_10_keyed(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                     const uint32_t (&k0)[10], const uint32_t (&k1)[10]) {
+#pragma unroll
+    for (int i = 0; i < 10; i++) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0[i];
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1[i];
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
+        c0 = n0;
+        c2 = n2;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
 // Random bytes of block `blk`: key = seed, counter = (blk, offset).
 __device__ __forceinline__ uint4 block_random(uint64_t seed, uint64_t offset, uint64_t blk) {
     return philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)offset, (uint32_t)(offset >> 32),

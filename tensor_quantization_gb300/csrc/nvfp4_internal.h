@@ -20,6 +20,10 @@ struct QArgs {
     uint32_t *workspace;  // [0] running max bits, [1] CTA ticket, [2] status
     uint32_t sign_mask;
     uint64_t seed, offset;
+    // Philox4x32-10 round keys of `seed` (key + round * Weyl constant),
+    // precomputed on the host so that kernels read them from the parameter
+    // bank instead of recomputing them for every block.
+    uint32_t round_key0[10], round_key1[10];
     int swizzled;
     int want_row, want_col;
 };

@@ -150,7 +150,11 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
                         f2 v[8];
                         unpack(raw, v);
                         uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
-                        if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, row * CS + j0 + b);
+                        if (MODE == MODE_SR) {
+                            const uint32_t blk = row * CS + j0 + b;  // < 2^30: high word 0
+                            rnd = philox4x32_10_keyed(blk, 0u, (uint32_t)a.offset, (uint32_t)(a.offset >> 32),
+                                                      a.round_key0, a.round_key1);
+                        }
                         c[b] = encode_block_fast<MODE, RHT>(v, sd, tab, signs, rnd, S[b]);
                     }
                 }
