@@ -14,11 +14,13 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tma.cuh"
 
 namespace nvfp4 {
 
 __device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, bool rht) {
     __shared__ uint32_t red[32];
+    allow_dependents();  // the quantize pass may start staging its tiles
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) {
         atomicMax(&a.workspace[0], m);

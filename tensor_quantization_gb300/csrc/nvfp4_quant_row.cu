@@ -113,13 +113,15 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
             if (t < ntiles) issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], t / ntc, t % ntc);
         }
     }
-    // per-scale state, built while the first copies are in flight
+    // per-scale state, built while the first copies are in flight; the amax
+    // pass may still be running until grid_dependency_wait returns
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
+    grid_dependency_wait();
     const float g = global_scale_of(a.amax[0]);
     build_table(tab, g, tid, blockDim.x);
-    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
     const ScaleDiv sd = make_scale_div(g);
     const bool fast = scale_all_fast(g);  // uniform: every divisor in the fast range
-    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
     if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
     __syncthreads();
 
@@ -297,8 +299,19 @@ static cudaError_t run_row(const QArgs &a, cudaStream_t s) {
     const int64_t tiles = ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int grid = (int)(tiles < cap ? tiles : cap);
-    k<<<grid, kTileRows, smem, s>>>(map, a);
-    return cudaGetLastError();
+    // programmatic dependent launch: the kernel stages its first tiles while
+    // the amax pass finishes, and waits for it before reading the amax
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTileRows);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, map, a);
 }
 
 template <int MODE, bool RHT, typename T>

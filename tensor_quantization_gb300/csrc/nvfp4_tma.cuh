@@ -66,6 +66,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor finishes; it must execute
+// grid_dependency_wait() before touching anything the predecessor writes.
+// The predecessor calls allow_dependents() once the rest of its work no longer
+// needs the SMs to itself.  Both are no-ops without such a launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Record of a device-side wait that gave up in this translation unit (0 =
 // none); kernels also poison their published global scale with NaN.
 static __device__ uint32_t g_wait_timeouts = 0;
