@@ -144,6 +144,18 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
             uint32_t S[4] = {0u, 0u, 0u, 0u};
             uint2 c[4];
             if (fast) {
+                // the four blocks' random words first: independent integer work
+                // the scheduler can interleave with the butterflies and divisions
+                uint4 rnd[4];
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    rnd[b] = make_uint4(0u, 0u, 0u, 0u);
+                    if (MODE == MODE_SR) {
+                        const uint32_t blk = row * CS + j0 + b;  // < 2^30: high word 0
+                        rnd[b] = philox4x32_10_keyed(blk, 0u, (uint32_t)a.offset, (uint32_t)(a.offset >> 32),
+                                                     a.round_key0, a.round_key1);
+                    }
+                }
 #pragma unroll
                 for (int b = 0; b < 4; b++) {
                     if (j0 + b < CS) {
@@ -151,13 +163,7 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
                         stage_block<T>(stage, tid, b, raw);
                         f2 v[8];
                         unpack(raw, v);
-                        uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
-                        if (MODE == MODE_SR) {
-                            const uint32_t blk = row * CS + j0 + b;  // < 2^30: high word 0
-                            rnd = philox4x32_10_keyed(blk, 0u, (uint32_t)a.offset, (uint32_t)(a.offset >> 32),
-                                                      a.round_key0, a.round_key1);
-                        }
-                        c[b] = encode_block_fast<MODE, RHT>(v, sd, tab, signs, rnd, S[b]);
+                        c[b] = encode_block_fast<MODE, RHT>(v, sd, tab, signs, rnd[b], S[b]);
                     }
                 }
             } else {
