@@ -276,6 +276,118 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled(const QArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------
+// Per-row global scale, the row staged in shared memory.  A CTA owns whole
+// rows: one bulk copy brings a row in (double-buffered across the CTA's rows),
+// pass 1 reduces its amax from shared memory, thread 0 publishes amax and g,
+// the CTA builds that row's divisor table, and pass 2 encodes from shared
+// memory with the same block encoders as the per-tensor kernel.
+constexpr int kRowBufs = 2;
+constexpr uint32_t kMaxStagedRowBytes = 96u * 1024u;  // per buffer
+
+template <typename T>
+__device__ __forceinline__ void smem_row_block(const uint8_t *rowp, uint32_t j, RawBlock<T> &b) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(rowp + (size_t)j * 16 * sizeof(T));
+#pragma unroll
+    for (int k = 0; k < (int)sizeof(T); k++) b.w[k] = p[k];
+}
+
+template <int MODE, bool RHT, typename T>
+__global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, uint32_t buf_bytes) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ DivTable tab;
+    __shared__ RhtMult rm;
+    __shared__ uint32_t red[32];
+    __shared__ __align__(8) uint64_t full[kRowBufs];
+    uint8_t *bufs = dyn_smem + ((16u - (smem_addr(dyn_smem) & 15u)) & 15u);
+    const uint32_t CS = (uint32_t)(a.cols >> 4);
+    const uint32_t csp = (CS + 3) & ~3u;
+    const uint32_t row_bytes = (uint32_t)a.cols * sizeof(T);
+    const bool words = (CS & 3u) == 0 && (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
+    const int tid = threadIdx.x;
+    const char *x = static_cast<const char *>(a.x);
+    if (tid == 0) {
+        for (int s = 0; s < kRowBufs; s++) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int k = 0; k < kRowBufs; k++) {
+            const int64_t r = blockIdx.x + (int64_t)k * gridDim.x;
+            if (r < a.rows) {
+                mbar_arrive_expect_tx(&full[k], row_bytes);
+                bulk_load(bufs + k * buf_bytes, x + r * a.ld * (int64_t)sizeof(T), row_bytes, &full[k]);
+            }
+        }
+    }
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
+    __syncthreads();
+    for (uint32_t k = 0;; ++k) {
+        const int64_t r = blockIdx.x + (int64_t)k * gridDim.x;
+        if (r >= a.rows) break;
+        const uint32_t s = k % kRowBufs;
+        const bool arrived = mbar_wait(&full[s], (k / kRowBufs) & 1u);
+        if (!arrived) atomicAdd(&g_wait_timeouts, 1u);
+        const uint8_t *rowp = bufs + s * buf_bytes;
+        // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max)
+        float m = 0.0f;
+        for (uint32_t j = tid; j < CS; j += blockDim.x) {
+            RawBlock<T> raw;
+            smem_row_block<T>(rowp, j, raw);
+            f2 v[8];
+            unpack(raw, v);
+            if (RHT) fwht16(v);
+            m = absmax_nan(m, block_amax(v));
+        }
+        float A = __uint_as_float(block_max_u32(__float_as_uint(m), red));
+        if (RHT) A = __fmul_rn(A, 0.25f);
+        const float g = global_scale_of(A);
+        build_table(tab, g, tid, blockDim.x);
+        const ScaleDiv sd = make_scale_div(g);
+        const bool fast = scale_all_fast(g);
+        // a row whose copy never arrived is published with a NaN scale
+        const bool lost = __syncthreads_or(!arrived);
+        if (tid == 0) {
+            a.amax[r] = A;
+            a.gscale[r] = lost ? __uint_as_float(0x7FFFFFFFu) : g;
+        }
+        // pass 2: encode (warp-uniform trip count for the scale-word shuffles)
+        for (uint32_t base = tid & ~31u; base < CS; base += blockDim.x) {
+            const uint32_t j = base + (tid & 31u);
+            const bool active = j < CS;
+            uint32_t S = 0;
+            if (active) {
+                RawBlock<T> raw;
+                smem_row_block<T>(rowp, j, raw);
+                f2 v[8];
+                unpack(raw, v);
+                uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+                if (MODE == MODE_SR) {
+                    const uint64_t blk = (uint64_t)r * CS + j;
+                    rnd = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
+                                              (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
+                }
+                uint2 c;
+                if (fast) {
+                    c = encode_block_fast<MODE, RHT>(v, sd, tab, signs, rnd, S);
+                } else {
+                    if (RHT) rht16(v, rm);
+                    c = encode_block<MODE>(v, sd, tab, rnd, S);
+                }
+                *reinterpret_cast<uint2 *>(a.codes_row + r * (a.cols >> 1) + 8 * j) = c;
+            }
+            store_scale(a, a.scales_row, S, (uint32_t)r, j, CS, csp, active, words);
+        }
+        __syncthreads();  // done with buffer s and the table
+        if (tid == 0) {
+            const int64_t rn = r + (int64_t)kRowBufs * gridDim.x;
+            if (rn < a.rows) {
+                fence_async_shared();
+                mbar_arrive_expect_tx(&full[s], row_bytes);
+                bulk_load(bufs + s * buf_bytes, x + rn * a.ld * (int64_t)sizeof(T), row_bytes, &full[s]);
+            }
+        }
+    }
+}
+
 template <typename K>
 static int grid_for(K kernel, int threads, int64_t work_items) {
     int per_sm = 0;
@@ -321,7 +433,23 @@ static cudaError_t run_row(const QArgs &a, cudaStream_t s) {
 }
 
 template <int MODE, bool RHT, typename T>
+static cudaError_t run_rowscaled_staged(const QArgs &a, cudaStream_t s) {
+    auto k = k_quant_rowscaled_staged<MODE, RHT, T>;
+    const uint32_t buf = ((uint32_t)(a.cols * sizeof(T)) + 15u) & ~15u;
+    const int smem = (int)(kRowBufs * buf + 16);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, smem);
+    const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+    const int grid = (int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
+    k<<<grid, 256, smem, s>>>(a, buf);
+    return cudaGetLastError();
+}
+
+template <int MODE, bool RHT, typename T>
 static cudaError_t run_rowscaled(const QArgs &a, cudaStream_t s) {
+    if ((uint64_t)a.cols * sizeof(T) <= kMaxStagedRowBytes) return run_rowscaled_staged<MODE, RHT, T>(a, s);
     auto k = k_quant_rowscaled<MODE, RHT, T>;
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0);
