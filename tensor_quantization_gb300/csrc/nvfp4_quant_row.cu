@@ -1,13 +1,18 @@
 // nvfp4_quant_row.cu -- rowwise 1x16 quantize kernels.
 //
-//  k_quant_row        per-tensor global scale (amax from the amax pass or
-//                     given by the caller).  Each CTA encodes one contiguous
-//                     range of 16-element blocks, a thread one block per
-//                     step, with the next block's loads issued before the
-//                     current one is encoded.
-//  k_quant_rowscaled  one global scale per row: a CTA owns a row, reduces its
-//                     amax, prepares that row's divisor table, then encodes
-//                     it (single launch, no separate amax pass).
+//  k_quant_row               per-tensor global scale (amax from the amax pass
+//                            or given by the caller).  TMA brings 64-row
+//                            tiles into shared memory; a thread encodes the
+//                            four blocks of one tile row.
+//  k_quant_rowscaled_staged  one global scale per row, rows of up to 96 KiB:
+//                            a CTA stages whole rows in shared memory with
+//                            bulk copies, reduces each row's amax, prepares
+//                            that row's divisors, then encodes it (single
+//                            launch, no separate amax pass).
+//  k_quant_rowscaled         the same for longer rows, reading global memory
+//                            twice (amax pass, then encode).
+#include <algorithm>
+
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
@@ -278,12 +283,20 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled(const QArgs a) {
 
 // ---------------------------------------------------------------------
 // Per-row global scale, the row staged in shared memory.  A CTA owns whole
-// rows: one bulk copy brings a row in (double-buffered across the CTA's rows),
-// pass 1 reduces its amax from shared memory, thread 0 publishes amax and g,
-// the CTA builds that row's divisor table, and pass 2 encodes from shared
-// memory with the same block encoders as the per-tensor kernel.
+// rows: one bulk copy brings a row in (two buffers, the next-but-one row is
+// requested as soon as every thread is past the row that used its buffer),
+// pass 1 reduces the row amax from shared memory, the CTA prepares that row's
+// 128 element divisors and the two block-scale divisors, and pass 2 encodes
+// from shared memory with the same block encoders as the per-tensor kernel.
+// Tables and reduction slots alternate between rows, so a row costs two CTA
+// barriers.  About four blocks per thread amortise the per-row preparation.
 constexpr int kRowBufs = 2;
 constexpr uint32_t kMaxStagedRowBytes = 96u * 1024u;  // per buffer
+
+struct RowTables {
+    DivTable t;
+    Divisor m6, m4;
+};
 
 template <typename T>
 __device__ __forceinline__ void smem_row_block(const uint8_t *rowp, uint32_t j, RawBlock<T> &b) {
@@ -292,19 +305,47 @@ __device__ __forceinline__ void smem_row_block(const uint8_t *rowp, uint32_t j, 
     for (int k = 0; k < (int)sizeof(T); k++) b.w[k] = p[k];
 }
 
+// max |x| bits over a staged row without the RHT: any element order will do,
+// so threads read consecutive 16-byte words (no bank conflicts) and compare
+// magnitude bits as unsigned integers (bf16: two 16-bit lanes per word).
+// NaN patterns sort above +inf, so a NaN wins as in the bit-max definition.
+template <typename T>
+__device__ __forceinline__ uint32_t row_bits_max(const uint8_t *rowp, uint32_t words16, int tid, int nt) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(rowp);
+    if (sizeof(T) == 2) {
+        uint32_t m = 0;
+        for (uint32_t i = tid; i < words16; i += nt) {
+            const uint4 w = p[i];
+            uint32_t t0, t1;
+            asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(w.x & 0x7FFF7FFFu), "r"(w.y & 0x7FFF7FFFu));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(t1) : "r"(w.z & 0x7FFF7FFFu), "r"(w.w & 0x7FFF7FFFu));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(t0), "r"(t1));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(t0));
+        }
+        return max(m & 0xFFFFu, m >> 16) << 16;
+    } else {
+        uint32_t m = 0;
+        for (uint32_t i = tid; i < words16; i += nt) {
+            const uint4 w = p[i];
+            m = max(m, max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu), max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu)));
+        }
+        return m;
+    }
+}
+
 template <int MODE, bool RHT, typename T>
 __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, uint32_t buf_bytes) {
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ DivTable tab;
+    __shared__ RowTables tabs[2];
     __shared__ RhtMult rm;
-    __shared__ uint32_t red[32];
+    __shared__ uint32_t red[2][8];
     __shared__ __align__(8) uint64_t full[kRowBufs];
     uint8_t *bufs = dyn_smem + ((16u - (smem_addr(dyn_smem) & 15u)) & 15u);
     const uint32_t CS = (uint32_t)(a.cols >> 4);
     const uint32_t csp = (CS + 3) & ~3u;
     const uint32_t row_bytes = (uint32_t)a.cols * sizeof(T);
     const bool words = (CS & 3u) == 0 && (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
     const char *x = static_cast<const char *>(a.x);
     if (tid == 0) {
         for (int s = 0; s < kRowBufs; s++) mbar_init(&full[s], 1);
@@ -323,35 +364,66 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
     for (uint32_t k = 0;; ++k) {
         const int64_t r = blockIdx.x + (int64_t)k * gridDim.x;
         if (r >= a.rows) break;
-        const uint32_t s = k % kRowBufs;
+        const uint32_t s = k % kRowBufs, par = k & 1u;
         const bool arrived = mbar_wait(&full[s], (k / kRowBufs) & 1u);
         if (!arrived) atomicAdd(&g_wait_timeouts, 1u);
         const uint8_t *rowp = bufs + s * buf_bytes;
         // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max)
-        float m = 0.0f;
-        for (uint32_t j = tid; j < CS; j += blockDim.x) {
-            RawBlock<T> raw;
-            smem_row_block<T>(rowp, j, raw);
-            f2 v[8];
-            unpack(raw, v);
-            if (RHT) fwht16(v);
-            m = absmax_nan(m, block_amax(v));
+        uint32_t mb;
+        if (RHT) {
+            float m = 0.0f;
+            for (uint32_t j = tid; j < CS; j += nt) {
+                RawBlock<T> raw;
+                smem_row_block<T>(rowp, j, raw);
+                f2 v[8];
+                unpack(raw, v);
+                fwht16(v);
+                m = absmax_nan(m, block_amax(v));
+            }
+            mb = __float_as_uint(m) & 0x7FFFFFFFu;
+        } else {
+            mb = row_bits_max<T>(rowp, row_bytes >> 4, tid, nt);
         }
-        float A = __uint_as_float(block_max_u32(__float_as_uint(m), red));
+        mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+        if (lane == 0) red[par][warp] = mb;
+        __syncthreads();  // (1) reduction slots; every thread is past row k-1
+        mb = lane < (nt >> 5) ? red[par][lane] : 0u;
+        mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+        if (tid == 0) {
+            // the buffer of row k-1 is free: request row k+1 into it
+            const int64_t rn = r + (int64_t)(kRowBufs - 1) * gridDim.x;
+            if (k > 0 && rn < a.rows) {
+                const uint32_t sn = (k + kRowBufs - 1) % kRowBufs;
+                fence_async_shared();
+                mbar_arrive_expect_tx(&full[sn], row_bytes);
+                bulk_load(bufs + sn * buf_bytes, x + rn * a.ld * (int64_t)sizeof(T), row_bytes, &full[sn]);
+            }
+        }
+        float A = __uint_as_float(mb);
         if (RHT) A = __fmul_rn(A, 0.25f);
         const float g = global_scale_of(A);
-        build_table(tab, g, tid, blockDim.x);
-        const ScaleDiv sd = make_scale_div(g);
-        const bool fast = scale_all_fast(g);
+        RowTables &tb = tabs[par];
+        for (int e = tid; e < 130; e += nt) {
+            if (e < 128)
+                tb.t.e[e] = make_divisor(__fmul_rn(e4m3_value((uint32_t)e), g));
+            else
+                (e == 128 ? tb.m6 : tb.m4) = make_divisor(__fmul_rn(e == 128 ? 6.0f : 4.0f, g));
+        }
         // a row whose copy never arrived is published with a NaN scale
-        const bool lost = __syncthreads_or(!arrived);
+        const bool lost = __syncthreads_or(!arrived);  // (2) tables ready
         if (tid == 0) {
             a.amax[r] = A;
             a.gscale[r] = lost ? __uint_as_float(0x7FFFFFFFu) : g;
         }
+        ScaleDiv sd;
+        sd.m6 = tb.m6;
+        sd.m4 = tb.m4;
+        sd.fast6 = divisor_fast(sd.m6.d);
+        sd.fast4 = divisor_fast(sd.m4.d);
+        const bool fast = scale_all_fast(g);
         // pass 2: encode (warp-uniform trip count for the scale-word shuffles)
-        for (uint32_t base = tid & ~31u; base < CS; base += blockDim.x) {
-            const uint32_t j = base + (tid & 31u);
+        for (uint32_t base = tid & ~31u; base < CS; base += nt) {
+            const uint32_t j = base + lane;
             const bool active = j < CS;
             uint32_t S = 0;
             if (active) {
@@ -367,23 +439,14 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
                 }
                 uint2 c;
                 if (fast) {
-                    c = encode_block_fast<MODE, RHT>(v, sd, tab, signs, rnd, S);
+                    c = encode_block_fast<MODE, RHT>(v, sd, tb.t, signs, rnd, S);
                 } else {
                     if (RHT) rht16(v, rm);
-                    c = encode_block<MODE>(v, sd, tab, rnd, S);
+                    c = encode_block<MODE>(v, sd, tb.t, rnd, S);
                 }
                 *reinterpret_cast<uint2 *>(a.codes_row + r * (a.cols >> 1) + 8 * j) = c;
             }
             store_scale(a, a.scales_row, S, (uint32_t)r, j, CS, csp, active, words);
-        }
-        __syncthreads();  // done with buffer s and the table
-        if (tid == 0) {
-            const int64_t rn = r + (int64_t)kRowBufs * gridDim.x;
-            if (rn < a.rows) {
-                fence_async_shared();
-                mbar_arrive_expect_tx(&full[s], row_bytes);
-                bulk_load(bufs + s * buf_bytes, x + rn * a.ld * (int64_t)sizeof(T), row_bytes, &full[s]);
-            }
         }
     }
 }
@@ -439,11 +502,14 @@ static cudaError_t run_rowscaled_staged(const QArgs &a, cudaStream_t s) {
     const int smem = (int)(kRowBufs * buf + 16);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // about four blocks of a row per thread, 32..256 threads
+    const int64_t cs = a.cols >> 4;
+    const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, ((cs + 3) / 4 + 31) / 32 * 32));
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
     const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
     const int grid = (int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
-    k<<<grid, 256, smem, s>>>(a, buf);
+    k<<<grid, threads, smem, s>>>(a, buf);
     return cudaGetLastError();
 }
 

@@ -203,6 +203,36 @@ def test_per_row(mode, swizzled, dtype):
     assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_per_row_many_rows_per_cta(mode):
+    """Enough rows that every CTA of the staged per-row kernel cycles through
+    its row buffers and table slots several times; output rows are compared
+    in bands spread over the tensor (the oracle's row range keeps it quick)."""
+    rows, cols = 6000, 4096
+    x = mixed_input(rows, cols, seed=17)
+    x[2999, 77] = float("nan")  # poisons only its own row
+    kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", per_row=True, sign_mask=0x5A3C,
+              seed=21, offset=2)
+    g = gpu_run(x, **kw)
+    for r0, r1 in [(0, 96), (2960, 3040), (rows - 96, rows)]:
+        o = oracle_run(x, row_range=(r0, r1), **kw)
+        assert np.array_equal(g["codes_row"][r0:r1], o["codes_row"][r0:r1]), (mode, r0)
+        assert np.array_equal(g["scales_row"].reshape(rows, -1)[r0:r1], o["scales_row"].reshape(rows, -1)[r0:r1])
+        assert same_float_bits(g["amax"][r0:r1], o["amax"][r0:r1])
+        assert same_float_bits(g["global_scale"][r0:r1], o["global_scale"][r0:r1])
+    assert np.isnan(g["global_scale"][2999]) and not np.isnan(g["global_scale"][2998])
+
+
+@pytest.mark.parametrize("mode", ["rne", "4o6"])
+def test_per_row_long_rows(mode):
+    """fp32 rows of 128 KiB exceed the staged kernel's row buffer and take the
+    two-read kernel; 64 KiB bf16 rows still fit."""
+    for cols, dtype in ((32768, torch.float32), (32768, torch.bfloat16)):
+        x = mixed_input(12, cols, seed=18, dtype=dtype)
+        kw = dict(mode=mode, per_row=True, swizzled=True)
+        assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("swizzled", [False, True], ids=["linear", "swizzled"])
 def test_2d_tiles(swizzled, dtype):
