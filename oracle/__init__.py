@@ -76,6 +76,8 @@ def _lib():
         lib.ora_e2m1_sr_n.restype = None
         lib.ora_e4m3_rn_n.argtypes = [vp, i64, vp]
         lib.ora_e4m3_rn_n.restype = None
+        lib.ora_candidate_error_n.argtypes = [vp, vp, vp, vp, i64, vp]
+        lib.ora_candidate_error_n.restype = None
         lib.ora_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.ora_f32_to_bf16.restype = ctypes.c_uint16
         _LIB = lib
@@ -226,4 +228,16 @@ def e4m3_rn_array(s: np.ndarray) -> np.ndarray:
     s = np.ascontiguousarray(s, np.float32)
     out = np.zeros(s.size, np.uint8)
     _lib().ora_e4m3_rn_n(_ptr(s), s.size, _ptr(out))
+    return out
+
+
+def candidate_error_array(y: np.ndarray, codes: np.ndarray, S: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """Four-over-six squared-error of each 16-value block (y [n,16], codes
+    [n,16] 4-bit, block scale bytes S [n], global scales g [n])."""
+    y = np.ascontiguousarray(y, np.float32).reshape(-1, 16)
+    codes = np.ascontiguousarray(codes, np.int32).reshape(-1, 16)
+    S = np.ascontiguousarray(S, np.uint32).ravel()
+    g = np.ascontiguousarray(g, np.float32).ravel()
+    out = np.zeros(len(y), np.float32)
+    _lib().ora_candidate_error_n(_ptr(y), _ptr(codes), _ptr(S), _ptr(g), len(y), _ptr(out))
     return out

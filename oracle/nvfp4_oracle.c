@@ -459,3 +459,13 @@ void ora_e2m1_sr_n(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
 void ora_e4m3_rn_n(const float *s, int64_t n, uint8_t *out) {
     for (int64_t i = 0; i < n; i++) out[i] = (uint8_t)ora_e4m3_rn(s[i]);
 }
+/* Four-over-six candidate errors of n blocks: block b has values y[16b..],
+ * codes code[16b..] (4-bit), block scale S[b] and global scale g[b]. */
+void ora_candidate_error_n(const float *y, const int32_t *code, const uint32_t *S, const float *g, int64_t n,
+                           float *out) {
+    for (int64_t b = 0; b < n; b++) {
+        int c[16];
+        for (int i = 0; i < 16; i++) c[i] = code[16 * b + i];
+        out[b] = candidate_error(y + 16 * b, c, S[b], g[b]);
+    }
+}

@@ -108,26 +108,32 @@ __device__ __forceinline__ uint2 encode_with_scale(const f2 (&y)[8], uint32_t S,
 // Four-over-six candidate error: squared dequantization error, reduced by
 // the clamped shuffle-down tree (offsets 8, 4, 2, 1: lane i += lane i+off).
 // (PR #4852 description: pinned width-16 error reduction.)  Every product and
-// sum is a separate, individually rounded scalar operation: ptxas may fuse a
-// packed f32x2 multiply into a following packed add, which would round
-// y - val*d once instead of twice and break the pinned error (and with it
-// ties between candidates that dequantize identically).  d = 0 when S = 0.
+// sum must round on its own.  ptxas contracts a packed f32x2 multiply into a
+// packed add, subtract or FMA that consumes it, even with .rn on both, which
+// would round y - val*d (or a square plus its partner) once instead of twice
+// and change which candidate wins a near-tie.  So only the dequantized value
+// is a packed multiply, and it feeds an FMA as a multiplicand:
+//   t = RN(val*d);  e = RN(t*(-1) + y) = RN(y - t);  p = RN(e*e + 0)
+// (e*e >= 0, so adding +0 is exact), and the tree adds FMA results only.
+// A GPU test compares this with the oracle on a million blocks.  d = 0 when
+// S = 0.
 __device__ __forceinline__ float candidate_error(const f2 (&y)[8], uint2 codes, float d) {
-    float p[16];
+    const f2 dd{d, d}, m1{-1.0f, -1.0f}, z{0.0f, 0.0f};
+    f2 p[8];
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         const uint32_t w = (k < 4) ? codes.x : codes.y;
-        const f2 val = e2m1x2_value(w >> (8 * (k & 3)));
-        const float e0 = __fsub_rn(y[k].x, __fmul_rn(val.x, d));
-        const float e1 = __fsub_rn(y[k].y, __fmul_rn(val.y, d));
-        p[2 * k] = __fmul_rn(e0, e0);
-        p[2 * k + 1] = __fmul_rn(e1, e1);
+        const f2 e = fma2(mul2(e2m1x2_value(w >> (8 * (k & 3))), dd), m1, y[k]);
+        p[k] = fma2(e, e, z);
     }
+    // p[k] holds elements 2k, 2k+1: offsets 8, 4, 2 pair p[k] with p[k+4],
+    // p[k+2], p[k+1]; offset 1 adds the two halves of p[0]
 #pragma unroll
-    for (int off = 8; off >= 1; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < off; i++) p[i] = __fadd_rn(p[i], p[i + off]);
-    return p[0];
+    for (int k = 0; k < 4; k++) p[k] = add2(p[k], p[k + 4]);
+    p[0] = add2(p[0], p[2]);
+    p[1] = add2(p[1], p[3]);
+    p[0] = add2(p[0], p[1]);
+    return __fadd_rn(p[0].x, p[0].y);
 }
 
 // Encode one block in the given mode.  Returns the codes and writes S.

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "nvfp4_device.cuh"
+#include "nvfp4_encode.cuh"
 
 using namespace nvfp4;
 
@@ -100,7 +101,22 @@ __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *ba
     }
 }
 
+// Four-over-six candidate error of block i: values y[16i..], codes packed two
+// per byte (low nibble first) in codes[i], element divisor d[i].
+__global__ void k_cand_err(const float *y, const uint2 *codes, const float *d, int64_t n, float *out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    f2 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) v[k] = f2{y[16 * i + 2 * k], y[16 * i + 2 * k + 1]};
+    out[i] = candidate_error(v, codes[i], d[i]);
+}
+
 extern "C" {
+int probe_cand_err(const float *y, const uint2 *codes, const float *d, int64_t n, float *out) {
+    k_cand_err<<<(unsigned)((n + 255) / 256), 256>>>(y, codes, d, n, out);
+    return cudaDeviceSynchronize();
+}
 int probe_e2m1(const float *q, int64_t n, uint8_t *out) {
     k_e2m1<<<(unsigned)((n + 255) / 256), 256>>>(q, n, out);
     return cudaDeviceSynchronize();

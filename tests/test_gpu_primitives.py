@@ -4,7 +4,9 @@ The hardware casts (cvt.rn.satfinite.e2m1x2 / e4m3x2 and their decodes) are
 checked against the oracle's converters over dense sweeps of every binade they
 can see, which also fixes operand order, nibble order, NaN, -0 and
 saturation.  The per-block exact division is checked against CUDA's own IEEE
-division on random and near-midpoint quotients.
+division on random and near-midpoint quotients.  The four-over-six
+candidate error (every product and sum individually rounded, pinned tree
+order) is checked against the oracle's on a million blocks.
 """
 import ctypes
 import os
@@ -39,6 +41,7 @@ def probes(tmp_path_factory):
     lib.probe_e4m3_value.argtypes = [vp]
     lib.probe_e2m1_value.argtypes = [vp]
     lib.probe_div.argtypes = [u64, i64, i32, vp, vp]
+    lib.probe_cand_err.argtypes = [vp, vp, vp, i64, vp]
     return lib
 
 
@@ -134,3 +137,32 @@ def test_exact_division(probes, kind):
     for seed in range(8):
         assert probes.probe_div(seed + 100 * kind, n, kind, ptr(bad), ptr(first)) == 0
     assert int(bad.item()) == 0, first.cpu().numpy().reshape(-1, 3)[:4]
+
+
+def test_four_over_six_candidate_error_matches_oracle(probes):
+    """Bit-exact squared errors, so that no multiply is fused into the add or
+    subtract that follows it (that would change which candidate wins a
+    near-tie).  Half of the blocks carry the RNE codes of y/d (errors of a real
+    candidate), half random codes (every code value against every divisor)."""
+    n = 1 << 20
+    rng = np.random.default_rng(31)
+    y = (rng.standard_normal((n, 16)) * np.exp2(rng.integers(-30, 30, (n, 1)))).astype(np.float32)
+    S = rng.integers(1, 127, n).astype(np.uint32)
+    S[rng.random(n) < 0.01] = 0
+    g = np.exp2(rng.uniform(-40, 20, n)).astype(np.float32) * np.float32(1.0 + rng.random(n).astype(np.float32))
+    sf = np.array([oracle.e4m3_value(int(b)) for b in range(256)], np.float32)[S]
+    d = np.where(S == 0, np.float32(0), sf * g).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d[:, None] == 0, np.float32(0), y / d[:, None]).astype(np.float32)
+    codes = oracle.e2m1_rne_array(q).reshape(n, 16).astype(np.int32)
+    rand = rng.random(n) < 0.5
+    codes[rand] = rng.integers(0, 16, (int(rand.sum()), 16))
+    want = oracle.candidate_error_array(y, codes, S, g)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    yt, ct, dt = (torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (y, packed, d))
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    assert probes.probe_cand_err(ptr(yt), ptr(ct), ptr(dt), n, ptr(out)) == 0
+    got = out.cpu().numpy()
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    bad = np.flatnonzero(~same)
+    assert bad.size == 0, f"{bad.size} blocks differ, first {bad[:4].tolist()}: {got[bad[:4]]} vs {want[bad[:4]]}"
