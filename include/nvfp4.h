@@ -84,15 +84,40 @@ enum {
     NVFP4_BLOCK_2D = 4,      /* one scale per 16x16 tile, replicated to 1x16      */
     NVFP4_SCALE_PER_ROW = 8, /* one global scale per output row                   */
     NVFP4_SWIZZLED = 16,     /* SWIZZLE_32_4_4 scale layout (else linear)         */
-    NVFP4_AMAX_GIVEN = 32    /* out->amax already holds A: skip the amax pass     */
+    NVFP4_AMAX_GIVEN = 32,   /* out->amax already holds A: skip the amax pass     */
+    NVFP4_FAST_MATH = 64     /* q = y * RN(1/d) instead of the exact quotient     */
 };
 
+/* NVFP4_FAST_MATH replaces the correctly rounded element quotient q = y / d by
+ * the product y * RN(1/d) (one multiply instead of a four-operation exact
+ * division).  The product is within 1.5 ulp of the quotient, so an element's
+ * code can change only when q lies within that distance of a rounding
+ * threshold (RNE) or of a dither threshold (SR): about one element in 10^4
+ * on Gaussian data, never by more than one grid step, never its sign.  Global
+ * scale, block scales and the Philox stream are unchanged.  ("在 RTX 5090
+ * (SM120) 上补全 NVFP4 量化相关 kernel", fast-math note: at most 0.1% of the
+ * codes may differ, by at most one step.)  Not available with four-over-six
+ * (NVFP4_ERR_UNSUPPORTED): its candidate choice compares exact errors. */
+
 /* The input matrix X: rows x cols elements, row pitch ld elements (ld >= cols).
- * x must be 16-byte aligned and ld * element size a multiple of 16 bytes. */
+ * x must be 16-byte aligned and ld * element size a multiple of 16 bytes.
+ *
+ * row0, col0: where X sits inside the full tensor it was cut from (0, 0 for a
+ * whole tensor).  They only number the Philox counters, so that the shards of
+ * a tensor quantized separately (one per GPU, say) give exactly the codes of
+ * the whole tensor: a rowwise shard is a range of whole rows (col0 = 0; its
+ * blocks are numbered (row0 + r) * (cols / 16) + j) and a columnwise shard a
+ * range of whole columns (row0 = 0; blocks (col0 + c) * (rows / 16) + b).  A
+ * per-tensor amax must then be the whole tensor's (NVFP4_AMAX_GIVEN with the
+ * maximum over the shards); per-row scales need nothing.  Stochastic rounding
+ * with a nonzero offset along the other dimension returns
+ * NVFP4_ERR_UNSUPPORTED; round-to-nearest ignores row0 and col0.  Negative
+ * values are NVFP4_ERR_INVALID_ARG. */
 typedef struct {
     const void *x;
     int32_t dtype; /* nvfp4_dtype */
     int64_t rows, cols, ld;
+    int64_t row0, col0;
 } nvfp4_input;
 
 /* Output buffers (device pointers).  The pointers of an orientation that is

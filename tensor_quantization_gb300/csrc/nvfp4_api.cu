@@ -27,7 +27,7 @@ int sm_count() {
 namespace {
 
 constexpr uint32_t kKnownFlags = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_BLOCK_2D | NVFP4_SCALE_PER_ROW |
-                                 NVFP4_SWIZZLED | NVFP4_AMAX_GIVEN;
+                                 NVFP4_SWIZZLED | NVFP4_AMAX_GIVEN | NVFP4_FAST_MATH;
 constexpr int64_t kMaxDim = (int64_t)1 << 31;
 constexpr int64_t kMaxElems = (int64_t)1 << 34;
 
@@ -41,6 +41,7 @@ nvfp4_status check_input(const nvfp4_input *in) {
     if (in->dtype != NVFP4_IN_BF16 && in->dtype != NVFP4_IN_FP32) return NVFP4_ERR_INVALID_ARG;
     if (in->rows < 0 || in->cols < 0 || in->rows >= kMaxDim || in->cols >= kMaxDim) return NVFP4_ERR_INVALID_ARG;
     if (in->rows * in->cols > kMaxElems) return NVFP4_ERR_INVALID_ARG;
+    if (in->row0 < 0 || in->col0 < 0 || in->row0 >= kMaxDim || in->col0 >= kMaxDim) return NVFP4_ERR_INVALID_ARG;
     if (in->rows == 0 || in->cols == 0) return NVFP4_OK;
     if (!in->x || !aligned(in->x, 16)) return NVFP4_ERR_INVALID_ARG;
     if (in->ld < in->cols || (in->ld * elem_size(in->dtype)) % 16 != 0) return NVFP4_ERR_INVALID_ARG;
@@ -81,6 +82,10 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
     if (per_row && (want_col || given)) return NVFP4_ERR_UNSUPPORTED;
     if (rht && want_row && want_col) return NVFP4_ERR_UNSUPPORTED;
     if (rht && mode == nvfp4::MODE_4O6_ID) return NVFP4_ERR_UNSUPPORTED;
+    if ((flags & NVFP4_FAST_MATH) && mode == nvfp4::MODE_4O6_ID) return NVFP4_ERR_UNSUPPORTED;
+    // a stochastic shard is cut along its output rows only
+    if (mode == nvfp4::MODE_SR_ID && ((want_row && in->col0 != 0) || (want_col && in->row0 != 0)))
+        return NVFP4_ERR_UNSUPPORTED;
     if ((want_row || block2d) && in->cols % 16 != 0) return NVFP4_ERR_INVALID_ARG;
     if ((want_col || block2d) && in->rows % 16 != 0) return NVFP4_ERR_INVALID_ARG;
     const bool empty = in->rows == 0 || in->cols == 0;
@@ -111,7 +116,11 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
         a.round_key0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
         a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
     }
+    a.fast_math = (flags & NVFP4_FAST_MATH) ? 1 : 0;
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
+    const uint64_t base_row = (uint64_t)in->row0 * (uint64_t)(in->cols / 16);  // rowwise block numbers
+    const uint64_t base_col = (uint64_t)in->col0 * (uint64_t)(in->rows / 16);  // columnwise block numbers
+    a.blk_base = base_row;
     if (per_row) {
         st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, mode, rht, s));
     } else {
@@ -123,7 +132,10 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
             st = cuda_status(nvfp4::launch_quant_2d(a, fp32, s));
         } else {
             if (want_row) st = cuda_status(nvfp4::launch_quant_row(a, fp32, mode, rht, s));
-            if (st == NVFP4_OK && want_col) st = cuda_status(nvfp4::launch_quant_col(a, fp32, mode, rht, s));
+            if (st == NVFP4_OK && want_col) {
+                a.blk_base = base_col;
+                st = cuda_status(nvfp4::launch_quant_col(a, fp32, mode, rht, s));
+            }
         }
     }
     if (st != NVFP4_OK) return st;

@@ -174,7 +174,7 @@ __device__ __forceinline__ bool scale_all_fast(float g) {
 // below 2^-40 and keeps its sign, so its code cannot change) and the signs s_j
 // into the code-sign flip.  `signs` holds bit 4e+3 for every negated element
 // e of the 8 in one code word.
-template <bool SR>
+template <bool SR, bool AP = false>
 __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32_t S, bool fold4,
                                              uint2 signs, const uint4 &rnd) {
     if (fold4) {
@@ -184,8 +184,13 @@ __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32
         D.nrl = __fmul_rn(D.nrl, 0.25f);
     }
     f2 nq[8];
+    if (AP) {  // fast math: -(y * RN(1/d)), one multiply
 #pragma unroll
-    for (int k = 0; k < 8; k++) nq[k] = neg_quot2(v[k], D);
+        for (int k = 0; k < 8; k++) nq[k] = mul2(v[k], f2{D.nrh, D.nrh});
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; k++) nq[k] = neg_quot2(v[k], D);
+    }
     if (SR) {
 #pragma unroll
         for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], rbyte(rnd, 2 * k), rbyte(rnd, 2 * k + 1));
@@ -198,8 +203,9 @@ __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32
 }
 
 // One block on the fast path.  v holds the raw block (RHT: the butterfly is
-// applied here and the 0.25 / signs are folded as above).
-template <int MODE, bool RHT>
+// applied here and the 0.25 / signs are folded as above).  AP (fast math)
+// replaces the exact element quotient by y * RN(1/d); block scales stay exact.
+template <int MODE, bool RHT, bool AP = false>
 __device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &sd, const DivTable &T,
                                                    uint2 signs, const uint4 &rnd, uint32_t &S_out) {
     if (RHT) fwht16(v);
@@ -219,7 +225,7 @@ __device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &s
     } else {
         const uint32_t S = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m6));
         S_out = S;
-        return encode_fast<MODE == MODE_SR>(v, T.e[S], S, RHT, signs, rnd);
+        return encode_fast<MODE == MODE_SR, AP>(v, T.e[S], S, RHT, signs, rnd);
     }
 }
 

@@ -24,8 +24,12 @@ struct QArgs {
     // precomputed on the host so that kernels read them from the parameter
     // bank instead of recomputing them for every block.
     uint32_t round_key0[10], round_key1[10];
+    // global number of this launch's first block (shards of a larger
+    // tensor): added to every Philox block counter
+    uint64_t blk_base;
     int swizzled;
     int want_row, want_col;
+    int fast_math;  // element quotient as y * RN(1/d)
 };
 
 // Device properties, cached per device.
@@ -51,6 +55,12 @@ cudaError_t launch_quant_col(const QArgs &a, bool fp32, int mode, bool rht, cuda
 cudaError_t launch_quant_2d(const QArgs &a, bool fp32, cudaStream_t s);
 // Rowwise with one global scale per row, amax and quantize in one pass.
 cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+// The same launches with the fast-math element quotient (defined in their own
+// translation units).
+cudaError_t launch_quant_row_approx(const QArgs &a, bool fp32, int mode, bool rht, bool scaled_rows,
+                                    cudaStream_t s);
+cudaError_t launch_quant_col_approx(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+cudaError_t launch_quant_2d_approx(const QArgs &a, bool fp32, cudaStream_t s);
 // Zero the pad bytes of a swizzled scale array.
 cudaError_t launch_scale_pad(uint8_t *scales, int64_t rows_out, int64_t cs, cudaStream_t s);
 

@@ -1,0 +1,556 @@
+// nvfp4_quant_row.cuh -- rowwise 1x16 quantize kernels (included by
+// nvfp4_quant_row.cu for exact division and nvfp4_quant_row_approx.cu for
+// NVFP4_FAST_MATH; AP selects the element quotient, everything else is
+// shared).
+//
+//  k_quant_row               per-tensor global scale (amax from the amax pass
+//                            or given by the caller).  TMA brings 64-row
+//                            tiles into shared memory; a thread encodes the
+//                            four blocks of one tile row.
+//  k_quant_rowscaled_staged  one global scale per row, rows of up to 96 KiB:
+//                            a CTA stages whole rows in shared memory with
+//                            bulk copies, reduces each row's amax, prepares
+//                            that row's divisors, then encodes it (single
+//                            launch, no separate amax pass).
+//  k_quant_rowscaled         the same for longer rows, reading global memory
+//                            twice (amax pass, then encode).
+#pragma once
+
+#include <algorithm>
+
+#include "nvfp4_encode.cuh"
+#include "nvfp4_internal.h"
+#include "nvfp4_load.cuh"
+#include "nvfp4_tma.cuh"
+
+namespace nvfp4 {
+namespace {  // internal linkage: each including unit has its own kernels
+
+// Scale bytes of 4 consecutive blocks of a row go out as one 32-bit store
+// (lanes 4m..4m+3 hold blocks j..j+3 with j % 4 == 0); otherwise one byte.
+// Scale arrays stay below 4 GiB, so offsets are 32-bit.
+__device__ __forceinline__ void store_scale(const QArgs &a, uint8_t *scales, uint32_t S, uint32_t r, uint32_t j,
+                                            uint32_t CS, uint32_t csp, bool active, bool words) {
+    if (words) {
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, S, 1);
+        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, S, 2);
+        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, S, 3);
+        if (active && (j & 3u) == 0) {
+            const uint32_t off = a.swizzled ? swizzle_offset32(r, j, csp) : r * CS + j;
+            *reinterpret_cast<uint32_t *>(scales + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+    } else if (active) {
+        scales[a.swizzled ? swizzle_offset32(r, j, csp) : r * CS + j] = (uint8_t)S;
+    }
+}
+
+// Encode one block from its raw bytes (flat block index i, for the Philox
+// counter); returns the codes and writes S.
+template <int MODE, bool RHT, typename T>
+__device__ __forceinline__ uint2 row_block(const QArgs &a, const ScaleDiv &sd, const DivTable &tab, const RhtMult &rm,
+                                           const RawBlock<T> &raw, uint32_t i, uint32_t &S) {
+    f2 v[8];
+    unpack(raw, v);
+    if (RHT) rht16(v, rm);
+    uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+    if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, a.blk_base + i);
+    return encode_block<MODE>(v, sd, tab, rnd, S);
+}
+
+// ---------------------------------------------------------------------
+// Per-tensor rowwise quantize, input staged through shared memory by TMA.
+//
+// The input is cut into tiles of 64 rows x 64 columns (4 blocks per row).
+// One thread owns one tile row, i.e. 4 consecutive blocks: its codes are 32
+// contiguous bytes and its scales one 32-bit word.  Persistent CTAs walk the
+// tiles round-robin; thread 0 keeps kStages tiles in flight with TMA copies
+// into 128-byte-swizzled buffers, so the 16-byte chunks a warp reads sit in
+// distinct bank groups.  Boxes outside the tensor are zero-filled, which also
+// yields the zero pad bytes of the swizzled scale layout.
+constexpr int kTileRows = 64;
+constexpr int kTileCols = 64;
+constexpr int kStages = 1;
+
+template <typename T>
+struct RowTile {
+    static constexpr int kBoxCols = 128 / (int)sizeof(T);  // one 128-byte swizzle span
+    static constexpr int kBoxes = kTileCols / kBoxCols;    // 1 (bf16) or 2 (fp32)
+    static constexpr int kBoxBytes = kTileRows * 128;
+    static constexpr int kStageBytes = kBoxes * kBoxBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+};
+
+// Raw bytes of block b (0..3) of tile row `row`: chunk c of a 128-byte box
+// row is stored at chunk position c ^ (row % 8).
+template <typename T>
+__device__ __forceinline__ void stage_block(const uint8_t *stage, int row, int b, RawBlock<T> &raw) {
+    constexpr int kChunks = (int)sizeof(T);  // 16-byte chunks per block
+    constexpr int kPerBoxRow = 8 / kChunks;  // blocks per box row
+    const uint8_t *base = stage + (b / kPerBoxRow) * RowTile<T>::kBoxBytes + row * 128;
+#pragma unroll
+    for (int k = 0; k < kChunks; k++) {
+        const int c = (b % kPerBoxRow) * kChunks + k;
+        raw.w[k] = *reinterpret_cast<const uint4 *>(base + ((c ^ (row & 7)) << 4));
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void issue_tile(const CUtensorMap *map, uint8_t *stage, uint64_t *bar, uint32_t tr,
+                                           uint32_t tc) {
+    mbar_arrive_expect_tx(bar, RowTile<T>::kStageBytes);
+#pragma unroll
+    for (int b = 0; b < RowTile<T>::kBoxes; b++)
+        tma_load_2d(stage + b * RowTile<T>::kBoxBytes, map, (int32_t)(tc * kTileCols + b * RowTile<T>::kBoxCols),
+                    (int32_t)(tr * kTileRows), bar);
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+__global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ DivTable tab;
+    __shared__ RhtMult rm;
+    __shared__ __align__(8) uint64_t full[kStages];
+    uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
+    const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, CS = C >> 4, csp = (CS + 3) & ~3u;
+    const uint32_t Rp = (R + 127) & ~127u;
+    const uint32_t ntc = (C + kTileCols - 1) / kTileCols, ntr = (R + kTileRows - 1) / kTileRows;
+    const uint32_t ntiles = ntc * ntr;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; s++) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int k = 0; k < kStages; k++) {
+            const uint32_t t = blockIdx.x + k * gridDim.x;
+            if (t < ntiles) issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], t / ntc, t % ntc);
+        }
+    }
+    // per-scale state, built while the first copies are in flight; the amax
+    // pass may still be running until grid_dependency_wait returns
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
+    grid_dependency_wait();
+    const float g = global_scale_of(a.amax[0]);
+    build_table(tab, g, tid, blockDim.x);
+    const ScaleDiv sd = make_scale_div(g);
+    const bool fast = scale_all_fast(g);  // uniform: every divisor in the fast range
+    if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
+    __syncthreads();
+
+    // vector stores only where every address is aligned for them
+    const bool codes16 = (C & 31u) == 0 && (reinterpret_cast<uintptr_t>(a.codes_row) & 15u) == 0;
+    const bool words = (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
+    const bool lin_words = words && (CS & 3u) == 0;
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t t = blockIdx.x + k * gridDim.x;
+        if (t >= ntiles) break;
+        const uint32_t s = k % kStages;
+        if (!mbar_wait(&full[s], (k / kStages) & 1u)) {  // a copy never landed: bounded, visible failure
+            atomicAdd(&g_wait_timeouts, 1u);
+            a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
+        }
+        const uint32_t tr = t / ntc, tc = t - tr * ntc;
+        const uint32_t row = tr * kTileRows + tid, j0 = tc * 4;
+        const uint8_t *stage = stages + s * RowTile<T>::kStageBytes;
+        if (row < R) {
+            uint32_t S[4] = {0u, 0u, 0u, 0u};
+            uint2 c[4];
+            if (fast) {
+                // the four blocks' random words first: independent integer work
+                // the scheduler can interleave with the butterflies and divisions
+                uint4 rnd[4];
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    rnd[b] = make_uint4(0u, 0u, 0u, 0u);
+                    if (MODE == MODE_SR) {
+                        const uint64_t blk = a.blk_base + (uint64_t)(row * CS + j0 + b);
+                        rnd[b] = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
+                                                     (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    if (j0 + b < CS) {
+                        RawBlock<T> raw;
+                        stage_block<T>(stage, tid, b, raw);
+                        f2 v[8];
+                        unpack(raw, v);
+                        c[b] = encode_block_fast<MODE, RHT, AP>(v, sd, tab, signs, rnd[b], S[b]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    if (j0 + b < CS) {
+                        RawBlock<T> raw;
+                        stage_block<T>(stage, tid, b, raw);
+                        c[b] = row_block<MODE, RHT, T>(a, sd, tab, rm, raw, row * CS + j0 + b, S[b]);
+                    }
+                }
+            }
+            uint8_t *codes = a.codes_row + (int64_t)row * (C >> 1) + j0 * 8;
+            if (codes16 && j0 + 3 < CS) {
+                reinterpret_cast<uint4 *>(codes)[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+                reinterpret_cast<uint4 *>(codes)[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++)
+                    if (j0 + b < CS) reinterpret_cast<uint2 *>(codes)[b] = c[b];
+            }
+            const uint32_t word = S[0] | (S[1] << 8) | (S[2] << 16) | (S[3] << 24);
+            if (a.swizzled) {
+                uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+                if (words) {
+                    *reinterpret_cast<uint32_t *>(dst) = word;
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 4; b++) dst[b] = (uint8_t)S[b];
+                }
+            } else if (lin_words && j0 + 3 < CS) {
+                *reinterpret_cast<uint32_t *>(a.scales_row + row * CS + j0) = word;
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++)
+                    if (j0 + b < CS) a.scales_row[row * CS + j0 + b] = (uint8_t)S[b];
+            }
+        } else if (a.swizzled && row < Rp) {  // pad rows of the swizzled layout
+            uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+            if (words) {
+                *reinterpret_cast<uint32_t *>(dst) = 0u;
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; b++) dst[b] = 0;
+            }
+        }
+        __syncthreads();  // every thread is done with stage s
+        if (tid == 0) {
+            const uint32_t tn = t + kStages * gridDim.x;
+            if (tn < ntiles) {
+                fence_async_shared();
+                issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], tn / ntc, tn % ntc);
+            }
+        }
+    }
+}
+
+template <int MODE, bool RHT, typename T>
+__global__ void __launch_bounds__(256) k_quant_rowscaled(const QArgs a) {
+    __shared__ DivTable tab;
+    __shared__ RhtMult rm;
+    __shared__ uint32_t red[32];
+    const uint32_t CS = (uint32_t)(a.cols >> 4);
+    const uint32_t csp = (CS + 3) & ~3u;
+    if (RHT) build_rht_mult(rm, a.sign_mask, threadIdx.x);
+    const bool words = (CS & 3u) == 0;
+    const T *x = static_cast<const T *>(a.x);
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        const T *xr = x + r * a.ld;
+        // pass 1: amax of the row (post-RHT magnitudes; the 0.25 is applied to
+        // the maximum, which rounds the same way because rounding is monotone)
+        float m = 0.0f;
+        for (uint32_t j = threadIdx.x; j < CS; j += blockDim.x) {
+            RawBlock<T> b;
+            load_raw(xr + 16 * j, b);
+            f2 v[8];
+            unpack(b, v);
+            if (RHT) fwht16(v);
+            m = absmax_nan(m, block_amax(v));
+        }
+        float A = __uint_as_float(block_max_u32(__float_as_uint(m), red));
+        if (RHT) A = __fmul_rn(A, 0.25f);
+        const float g = global_scale_of(A);
+        if (threadIdx.x == 0) {
+            a.amax[r] = A;
+            a.gscale[r] = g;
+        }
+        build_table(tab, g, threadIdx.x, blockDim.x);
+        const ScaleDiv sd = make_scale_div(g);
+        __syncthreads();
+        // pass 2: encode (warp-uniform trip count for the scale-word shuffles)
+        for (uint32_t base = threadIdx.x & ~31u; base < CS; base += blockDim.x) {
+            const uint32_t j = base + (threadIdx.x & 31u);
+            const bool active = j < CS;
+            uint32_t S = 0;
+            if (active) {
+                RawBlock<T> b;
+                load_raw(xr + 16 * j, b);
+                f2 v[8];
+                unpack(b, v);
+                if (RHT) rht16(v, rm);
+                uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+                if (MODE == MODE_SR) rnd = block_random(a.seed, a.offset, a.blk_base + (uint64_t)r * CS + j);
+                const uint2 c = encode_block<MODE>(v, sd, tab, rnd, S);
+                *reinterpret_cast<uint2 *>(a.codes_row + r * (a.cols >> 1) + 8 * j) = c;
+            }
+            store_scale(a, a.scales_row, S, (uint32_t)r, j, CS, csp, active, words);
+        }
+        __syncthreads();  // the next row rebuilds the table
+    }
+}
+
+// ---------------------------------------------------------------------
+// Per-row global scale, the row staged in shared memory.  A CTA owns whole
+// rows: one bulk copy brings a row in (two buffers, the next-but-one row is
+// requested as soon as every thread is past the row that used its buffer),
+// pass 1 reduces the row amax from shared memory, the CTA prepares that row's
+// 128 element divisors and the two block-scale divisors, and pass 2 encodes
+// from shared memory with the same block encoders as the per-tensor kernel.
+// Tables and reduction slots alternate between rows, so a row costs two CTA
+// barriers.  About four blocks per thread amortise the per-row preparation.
+constexpr int kRowBufs = 2;
+constexpr uint32_t kMaxStagedRowBytes = 96u * 1024u;  // per buffer
+
+struct RowTables {
+    DivTable t;
+    Divisor m6, m4;
+};
+
+template <typename T>
+__device__ __forceinline__ void smem_row_block(const uint8_t *rowp, uint32_t j, RawBlock<T> &b) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(rowp + (size_t)j * 16 * sizeof(T));
+#pragma unroll
+    for (int k = 0; k < (int)sizeof(T); k++) b.w[k] = p[k];
+}
+
+// max |x| bits over a staged row without the RHT: any element order will do,
+// so threads read consecutive 16-byte words (no bank conflicts) and compare
+// magnitude bits as unsigned integers (bf16: two 16-bit lanes per word).
+// NaN patterns sort above +inf, so a NaN wins as in the bit-max definition.
+template <typename T>
+__device__ __forceinline__ uint32_t row_bits_max(const uint8_t *rowp, uint32_t words16, int tid, int nt) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(rowp);
+    if (sizeof(T) == 2) {
+        uint32_t m = 0;
+        for (uint32_t i = tid; i < words16; i += nt) {
+            const uint4 w = p[i];
+            uint32_t t0, t1;
+            asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(w.x & 0x7FFF7FFFu), "r"(w.y & 0x7FFF7FFFu));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(t1) : "r"(w.z & 0x7FFF7FFFu), "r"(w.w & 0x7FFF7FFFu));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(t0), "r"(t1));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(t0));
+        }
+        return max(m & 0xFFFFu, m >> 16) << 16;
+    } else {
+        uint32_t m = 0;
+        for (uint32_t i = tid; i < words16; i += nt) {
+            const uint4 w = p[i];
+            m = max(m, max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu), max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu)));
+        }
+        return m;
+    }
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+__global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, uint32_t buf_bytes) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ RowTables tabs[2];
+    __shared__ RhtMult rm;
+    __shared__ uint32_t red[2][8];
+    __shared__ __align__(8) uint64_t full[kRowBufs];
+    uint8_t *bufs = dyn_smem + ((16u - (smem_addr(dyn_smem) & 15u)) & 15u);
+    const uint32_t CS = (uint32_t)(a.cols >> 4);
+    const uint32_t csp = (CS + 3) & ~3u;
+    const uint32_t row_bytes = (uint32_t)a.cols * sizeof(T);
+    const bool words = (CS & 3u) == 0 && (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const char *x = static_cast<const char *>(a.x);
+    if (tid == 0) {
+        for (int s = 0; s < kRowBufs; s++) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int k = 0; k < kRowBufs; k++) {
+            const int64_t r = blockIdx.x + (int64_t)k * gridDim.x;
+            if (r < a.rows) {
+                mbar_arrive_expect_tx(&full[k], row_bytes);
+                bulk_load(bufs + k * buf_bytes, x + r * a.ld * (int64_t)sizeof(T), row_bytes, &full[k]);
+            }
+        }
+    }
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
+    __syncthreads();
+    for (uint32_t k = 0;; ++k) {
+        const int64_t r = blockIdx.x + (int64_t)k * gridDim.x;
+        if (r >= a.rows) break;
+        const uint32_t s = k % kRowBufs, par = k & 1u;
+        const bool arrived = mbar_wait(&full[s], (k / kRowBufs) & 1u);
+        if (!arrived) atomicAdd(&g_wait_timeouts, 1u);
+        const uint8_t *rowp = bufs + s * buf_bytes;
+        // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max)
+        uint32_t mb;
+        if (RHT) {
+            float m = 0.0f;
+            for (uint32_t j = tid; j < CS; j += nt) {
+                RawBlock<T> raw;
+                smem_row_block<T>(rowp, j, raw);
+                f2 v[8];
+                unpack(raw, v);
+                fwht16(v);
+                m = absmax_nan(m, block_amax(v));
+            }
+            mb = __float_as_uint(m) & 0x7FFFFFFFu;
+        } else {
+            mb = row_bits_max<T>(rowp, row_bytes >> 4, tid, nt);
+        }
+        mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+        if (lane == 0) red[par][warp] = mb;
+        __syncthreads();  // (1) reduction slots; every thread is past row k-1
+        mb = lane < (nt >> 5) ? red[par][lane] : 0u;
+        mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+        if (tid == 0) {
+            // the buffer of row k-1 is free: request row k+1 into it
+            const int64_t rn = r + (int64_t)(kRowBufs - 1) * gridDim.x;
+            if (k > 0 && rn < a.rows) {
+                const uint32_t sn = (k + kRowBufs - 1) % kRowBufs;
+                fence_async_shared();
+                mbar_arrive_expect_tx(&full[sn], row_bytes);
+                bulk_load(bufs + sn * buf_bytes, x + rn * a.ld * (int64_t)sizeof(T), row_bytes, &full[sn]);
+            }
+        }
+        float A = __uint_as_float(mb);
+        if (RHT) A = __fmul_rn(A, 0.25f);
+        const float g = global_scale_of(A);
+        RowTables &tb = tabs[par];
+        for (int e = tid; e < 130; e += nt) {
+            if (e < 128)
+                tb.t.e[e] = make_divisor(__fmul_rn(e4m3_value((uint32_t)e), g));
+            else
+                (e == 128 ? tb.m6 : tb.m4) = make_divisor(__fmul_rn(e == 128 ? 6.0f : 4.0f, g));
+        }
+        // a row whose copy never arrived is published with a NaN scale
+        const bool lost = __syncthreads_or(!arrived);  // (2) tables ready
+        if (tid == 0) {
+            a.amax[r] = A;
+            a.gscale[r] = lost ? __uint_as_float(0x7FFFFFFFu) : g;
+        }
+        ScaleDiv sd;
+        sd.m6 = tb.m6;
+        sd.m4 = tb.m4;
+        sd.fast6 = divisor_fast(sd.m6.d);
+        sd.fast4 = divisor_fast(sd.m4.d);
+        const bool fast = scale_all_fast(g);
+        // pass 2: encode (warp-uniform trip count for the scale-word shuffles)
+        for (uint32_t base = tid & ~31u; base < CS; base += nt) {
+            const uint32_t j = base + lane;
+            const bool active = j < CS;
+            uint32_t S = 0;
+            if (active) {
+                RawBlock<T> raw;
+                smem_row_block<T>(rowp, j, raw);
+                f2 v[8];
+                unpack(raw, v);
+                uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+                if (MODE == MODE_SR) {
+                    const uint64_t blk = a.blk_base + (uint64_t)r * CS + j;
+                    rnd = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
+                                              (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
+                }
+                uint2 c;
+                if (fast) {
+                    c = encode_block_fast<MODE, RHT, AP>(v, sd, tb.t, signs, rnd, S);
+                } else {
+                    if (RHT) rht16(v, rm);
+                    c = encode_block<MODE>(v, sd, tb.t, rnd, S);
+                }
+                *reinterpret_cast<uint2 *>(a.codes_row + r * (a.cols >> 1) + 8 * j) = c;
+            }
+            store_scale(a, a.scales_row, S, (uint32_t)r, j, CS, csp, active, words);
+        }
+    }
+}
+
+template <typename K>
+int grid_for(K kernel, int threads, int64_t work_items) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t want = (work_items + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+cudaError_t run_row(const QArgs &a, cudaStream_t s) {
+    auto k = k_quant_row<MODE, RHT, T, AP>;
+    constexpr int smem = RowTile<T>::kSmemBytes;
+    static bool configured = false;  // one attribute call per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    CUtensorMap map;
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, RowTile<T>::kBoxCols, kTileRows))
+        return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTileRows, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t tiles = ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    // programmatic dependent launch: the kernel stages its first tiles while
+    // the amax pass finishes, and waits for it before reading the amax
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTileRows);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, map, a);
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+cudaError_t run_rowscaled_staged(const QArgs &a, cudaStream_t s) {
+    auto k = k_quant_rowscaled_staged<MODE, RHT, T, AP>;
+    const uint32_t buf = ((uint32_t)(a.cols * sizeof(T)) + 15u) & ~15u;
+    const int smem = (int)(kRowBufs * buf + 16);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // about four blocks of a row per thread, 32..256 threads
+    const int64_t cs = a.cols >> 4;
+    const int threads = (int)std::min<int64_t>(256, std::max<int64_t>(32, ((cs + 3) / 4 + 31) / 32 * 32));
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
+    const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+    const int grid = (int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
+    k<<<grid, threads, smem, s>>>(a, buf);
+    return cudaGetLastError();
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+cudaError_t run_rowscaled(const QArgs &a, cudaStream_t s) {
+    if ((uint64_t)a.cols * sizeof(T) <= kMaxStagedRowBytes) return run_rowscaled_staged<MODE, RHT, T, AP>(a, s);
+    auto k = k_quant_rowscaled<MODE, RHT, T>;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0);
+    const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+    const int grid = (int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
+    k<<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, bool AP>
+cudaError_t dispatch_row(const QArgs &a, int mode, bool rht, bool scaled_rows, cudaStream_t s) {
+    if (scaled_rows) {
+        if (mode == MODE_RNE) return rht ? run_rowscaled<MODE_RNE, true, T, AP>(a, s) : run_rowscaled<MODE_RNE, false, T, AP>(a, s);
+        if (mode == MODE_SR) return rht ? run_rowscaled<MODE_SR, true, T, AP>(a, s) : run_rowscaled<MODE_SR, false, T, AP>(a, s);
+        if constexpr (!AP) return run_rowscaled<MODE_4O6, false, T, false>(a, s);
+        return cudaErrorInvalidValue;  // four-over-six has no fast-math form
+    }
+    if (mode == MODE_RNE) return rht ? run_row<MODE_RNE, true, T, AP>(a, s) : run_row<MODE_RNE, false, T, AP>(a, s);
+    if (mode == MODE_SR) return rht ? run_row<MODE_SR, true, T, AP>(a, s) : run_row<MODE_SR, false, T, AP>(a, s);
+    if constexpr (!AP) return run_row<MODE_4O6, false, T, false>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+// Rowwise launches of one quotient kind (AP: fast math).
+template <bool AP>
+cudaError_t quant_row_launch(const QArgs &a, bool fp32, int mode, bool rht, bool scaled_rows, cudaStream_t s) {
+    return fp32 ? dispatch_row<float, AP>(a, mode, rht, scaled_rows, s)
+                : dispatch_row<bf16_t, AP>(a, mode, rht, scaled_rows, s);
+}
+
+}  // namespace
+}  // namespace nvfp4

@@ -22,7 +22,7 @@ _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 IN_BF16, IN_FP32 = 0, 1
-ROWWISE, COLWISE, BLOCK_2D, SCALE_PER_ROW, SWIZZLED, AMAX_GIVEN = 1, 2, 4, 8, 16, 32
+ROWWISE, COLWISE, BLOCK_2D, SCALE_PER_ROW, SWIZZLED, AMAX_GIVEN, FAST_MATH = 1, 2, 4, 8, 16, 32, 64
 
 
 class NVFP4Error(RuntimeError):
@@ -33,7 +33,8 @@ class NVFP4Error(RuntimeError):
 
 class Input(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
-                ("cols", ctypes.c_int64), ("ld", ctypes.c_int64)]
+                ("cols", ctypes.c_int64), ("ld", ctypes.c_int64), ("row0", ctypes.c_int64),
+                ("col0", ctypes.c_int64)]
 
 
 class Output(ctypes.Structure):
@@ -99,7 +100,9 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
 
 
-def make_input(x: torch.Tensor) -> Input:
+def make_input(x: torch.Tensor, row0: int = 0, col0: int = 0) -> Input:
+    """The C input descriptor of a 2-D tensor; (row0, col0) is its position in
+    the full tensor when it is a shard (Philox block numbering only)."""
     if x.dim() != 2:
         raise ValueError("input must be 2-D")
     if x.dtype == torch.bfloat16:
@@ -113,12 +116,16 @@ def make_input(x: torch.Tensor) -> Input:
     per16 = 16 // x.element_size()
     # a single row has no meaningful pitch: report the row length rounded up
     ld = x.stride(0) if x.size(0) > 1 else (x.size(1) + per16 - 1) // per16 * per16
-    return Input(x.data_ptr() if x.numel() else None, dt, x.size(0), x.size(1), ld)
+    return Input(x.data_ptr() if x.numel() else None, dt, x.size(0), x.size(1), ld, row0, col0)
 
 
 def make_output(codes_row=None, scales_row=None, codes_col=None, scales_col=None, amax=None,
                 global_scale=None) -> Output:
     return Output(*(_ptr(t) for t in (codes_row, scales_row, codes_col, scales_col, amax, global_scale)))
+
+
+def _input(x) -> Input:
+    return x if isinstance(x, Input) else make_input(x)
 
 
 def _check(status: int, what: str) -> None:
@@ -136,22 +143,22 @@ def nvfp4_scale_bytes(rows_out: int, cols_out: int, flags: int) -> int:
 
 
 def nvfp4_amax(x, flags, use_rht, sign_mask, out: Output, workspace, stream=None) -> None:
-    _check(load().nvfp4_amax(ctypes.byref(make_input(x)), flags, int(use_rht), sign_mask & 0xFFFF,
+    _check(load().nvfp4_amax(ctypes.byref(_input(x)), flags, int(use_rht), sign_mask & 0xFFFF,
                              ctypes.byref(out), _ptr(workspace), _stream(stream)), "nvfp4_amax")
 
 
 def nvfp4_quantize_rne(x, flags, out: Output, workspace, stream=None) -> None:
-    _check(load().nvfp4_quantize_rne(ctypes.byref(make_input(x)), flags, ctypes.byref(out),
+    _check(load().nvfp4_quantize_rne(ctypes.byref(_input(x)), flags, ctypes.byref(out),
                                      _ptr(workspace), _stream(stream)), "nvfp4_quantize_rne")
 
 
 def nvfp4_quantize_sr(x, flags, seed, offset, out: Output, workspace, stream=None) -> None:
-    _check(load().nvfp4_quantize_sr(ctypes.byref(make_input(x)), flags, seed, offset, ctypes.byref(out),
+    _check(load().nvfp4_quantize_sr(ctypes.byref(_input(x)), flags, seed, offset, ctypes.byref(out),
                                     _ptr(workspace), _stream(stream)), "nvfp4_quantize_sr")
 
 
 def nvfp4_quantize_rht_sr(x, flags, sign_mask, seed, offset, out: Output, workspace, stream=None) -> None:
-    _check(load().nvfp4_quantize_rht_sr(ctypes.byref(make_input(x)), flags, sign_mask & 0xFFFF, seed, offset,
+    _check(load().nvfp4_quantize_rht_sr(ctypes.byref(_input(x)), flags, sign_mask & 0xFFFF, seed, offset,
                                         ctypes.byref(out), _ptr(workspace), _stream(stream)),
            "nvfp4_quantize_rht_sr")
 
@@ -159,13 +166,13 @@ def nvfp4_quantize_rht_sr(x, flags, sign_mask, seed, offset, out: Output, worksp
 def nvfp4_quantize_rht_sr_static(x, flags, sign_mask, seed, offset, out: Output, stream=None) -> None:
     """RHT + SR quantize with the amax scratch held inside the library (for
     callers that cannot allocate device memory; see include/nvfp4.h)."""
-    _check(load().nvfp4_quantize_rht_sr_static(ctypes.byref(make_input(x)), flags, sign_mask & 0xFFFF, seed,
+    _check(load().nvfp4_quantize_rht_sr_static(ctypes.byref(_input(x)), flags, sign_mask & 0xFFFF, seed,
                                                offset, ctypes.byref(out), _stream(stream)),
            "nvfp4_quantize_rht_sr_static")
 
 
 def nvfp4_quantize_four_over_six(x, flags, out: Output, workspace, stream=None) -> None:
-    _check(load().nvfp4_quantize_four_over_six(ctypes.byref(make_input(x)), flags, ctypes.byref(out),
+    _check(load().nvfp4_quantize_four_over_six(ctypes.byref(_input(x)), flags, ctypes.byref(out),
                                                _ptr(workspace), _stream(stream)), "nvfp4_quantize_four_over_six")
 
 
@@ -225,25 +232,28 @@ def alloc_outputs(x: torch.Tensor, flags: int) -> Quantized:
 def quantize(x: torch.Tensor, *, mode: str = "rne", rowwise: bool = True, colwise: bool = False,
              block2d: bool = False, per_row: bool = False, swizzled: bool = False, rht: bool = False,
              sign_mask: int = 0, seed: int = 0, offset: int = 0, amax: torch.Tensor | None = None,
-             stream=None, out: Quantized | None = None) -> Quantized:
+             fast_math: bool = False, row0: int = 0, col0: int = 0, stream=None,
+             out: Quantized | None = None) -> Quantized:
     flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (BLOCK_2D if block2d else 0) | \
-        (SCALE_PER_ROW if per_row else 0) | (SWIZZLED if swizzled else 0) | (AMAX_GIVEN if amax is not None else 0)
+        (SCALE_PER_ROW if per_row else 0) | (SWIZZLED if swizzled else 0) | \
+        (AMAX_GIVEN if amax is not None else 0) | (FAST_MATH if fast_math else 0)
     q = out if out is not None else alloc_outputs(x, flags)
     if amax is not None:
         q.amax.copy_(amax)
     o = make_output(q.codes_row, q.scales_row, q.codes_col, q.scales_col, q.amax, q.global_scale)
     ws = Workspace.get(x.device)
+    xin = make_input(x, row0, col0)
     with torch.cuda.device(x.device):
         if rht:
             if mode != "sr":
                 raise ValueError("the RHT entry point rounds stochastically (mode='sr')")
-            nvfp4_quantize_rht_sr(x, flags, sign_mask, seed, offset, o, ws, stream)
+            nvfp4_quantize_rht_sr(xin, flags, sign_mask, seed, offset, o, ws, stream)
         elif mode == "rne":
-            nvfp4_quantize_rne(x, flags, o, ws, stream)
+            nvfp4_quantize_rne(xin, flags, o, ws, stream)
         elif mode == "sr":
-            nvfp4_quantize_sr(x, flags, seed, offset, o, ws, stream)
+            nvfp4_quantize_sr(xin, flags, seed, offset, o, ws, stream)
         elif mode == "4o6":
-            nvfp4_quantize_four_over_six(x, flags, o, ws, stream)
+            nvfp4_quantize_four_over_six(xin, flags, o, ws, stream)
         else:
             raise ValueError(f"unknown mode {mode}")
     return q

@@ -46,8 +46,8 @@ def test_host_only_queries(lib):
         assert nvfp4.status_string(s)
 
 
-def _inp(rows, cols, ld, ptr=16, dtype=0):
-    return nvfp4.Input(ptr, dtype, rows, cols, ld)
+def _inp(rows, cols, ld, ptr=16, dtype=0, row0=0, col0=0):
+    return nvfp4.Input(ptr, dtype, rows, cols, ld, row0, col0)
 
 
 def test_arguments_are_rejected_before_any_launch(lib):
@@ -73,6 +73,15 @@ def test_arguments_are_rejected_before_any_launch(lib):
         nvfp4.ERR_UNSUPPORTED
     rht = lib.nvfp4_quantize_rht_sr
     assert rht(ctypes.byref(_inp(16, 32, 32)), 3, 0, 1, 0, ctypes.byref(out), ws, None) == nvfp4.ERR_UNSUPPORTED
+    fo6 = lib.nvfp4_quantize_four_over_six
+    assert fo6(ctypes.byref(_inp(16, 32, 32)), 1 | nvfp4.FAST_MATH, ctypes.byref(out), ws, None) == \
+        nvfp4.ERR_UNSUPPORTED
+    # shard positions: never negative; a stochastic shard is cut along its output rows only
+    assert st(ctypes.byref(_inp(16, 32, 32, row0=-16)), 1, ctypes.byref(out), ws, None) == nvfp4.ERR_INVALID_ARG
+    assert sr(ctypes.byref(_inp(16, 32, 32, col0=32)), 1, 1, 0, ctypes.byref(out), ws, None) == \
+        nvfp4.ERR_UNSUPPORTED
+    assert sr(ctypes.byref(_inp(16, 32, 32, row0=16)), 2, 1, 0, ctypes.byref(out), ws, None) == \
+        nvfp4.ERR_UNSUPPORTED
     dq = lib.nvfp4_dequantize
     assert dq(16, 16, 16, 4, 24, 0, 16, 0, None) == nvfp4.ERR_INVALID_ARG  # cols % 16
     assert dq(16, 16, 16, 4, 32, 0, 16, 9, None) == nvfp4.ERR_INVALID_ARG  # dtype

@@ -397,3 +397,91 @@ def test_round_trip_through_the_library():
     err = (d.cpu() - x.float()).abs()
     assert math.isfinite(float(err.max()))
     assert float((err <= x.float().abs() * 0.25 + 1e-3 * x.float().abs().max()).float().mean()) > 0.99
+
+
+# ------------------------------------------------------------- fast math
+def _nibbles(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, np.uint8)
+    return np.stack([c & 15, c >> 4], -1).reshape(c.shape[0], -1)
+
+
+FAST_CASES = {
+    "row_rne": dict(mode="rne"),
+    "row_sr": dict(mode="sr", seed=3, offset=1),
+    "row_rht_sr": dict(mode="sr", rht=True, sign_mask=0x9C3A, seed=4, swizzled=True),
+    "col_rne": dict(mode="rne", rowwise=False, colwise=True),
+    "col_rht_sr": dict(mode="sr", rht=True, sign_mask=0x0FF0, seed=5, rowwise=False, colwise=True),
+    "both_sr": dict(mode="sr", colwise=True, seed=6),
+    "2d": dict(mode="rne", block2d=True, colwise=True),
+    "per_row_rht_sr": dict(mode="sr", rht=True, per_row=True, seed=7),
+}
+
+
+@pytest.mark.parametrize("case", list(FAST_CASES))
+def test_fast_math_codes_within_one_step(case):
+    """FAST_MATH keeps every scale, and changes at most 0.1% of the codes, each
+    to the neighbouring grid value of the same sign."""
+    x = mixed_input(512, 1024, seed=zlib.crc32(case.encode()) & 0xFFFF)
+    kw = FAST_CASES[case]
+    g, o = gpu_run(x, fast_math=True, **kw), oracle_run(x, **kw)
+    assert same_float_bits(g["amax"], o["amax"]) and same_float_bits(g["global_scale"], o["global_scale"])
+    for orient in ("row", "col"):
+        if f"codes_{orient}" not in o:
+            continue
+        assert np.array_equal(g[f"scales_{orient}"], o[f"scales_{orient}"]), orient
+        a, b = _nibbles(g[f"codes_{orient}"]), _nibbles(o[f"codes_{orient}"])
+        diff = a != b
+        assert diff.mean() <= 1e-3, (orient, diff.mean())
+        da, db = a[diff].astype(int), b[diff].astype(int)
+        assert np.all((da >> 3) == (db >> 3)) and np.all(np.abs((da & 7) - (db & 7)) == 1), orient
+
+
+# ------------------------------------------------- shards of one tensor
+def test_row_shards_reproduce_the_whole_tensor():
+    """Rowwise RHT + SR: shards of whole 128-row bands, each quantized with the
+    whole tensor's amax (the maximum of the shards' amax, as an all-reduce
+    would give) and its row offset, concatenate to the unsharded output."""
+    x = mixed_input(1024, 512, seed=21)
+    xd = to_device(x)
+    kw = dict(mode="sr", rht=True, sign_mask=0x6B2D, seed=8, offset=3, swizzled=True)
+    whole = gpu_run(x, x_dev=xd, **kw)
+    bounds = [0, 256, 640, 1024]
+    amaxes = []
+    for r0, r1 in zip(bounds[:-1], bounds[1:]):
+        a = torch.empty(1, device="cuda")
+        nvfp4.nvfp4_amax(xd[r0:r1], nvfp4.ROWWISE, True, kw["sign_mask"],
+                         nvfp4.make_output(amax=a, global_scale=torch.empty(1, device="cuda")),
+                         nvfp4.Workspace.get(xd.device))
+        amaxes.append(a)
+    A = torch.stack(amaxes).max().reshape(1)
+    cs_band = nvfp4.nvfp4_scale_bytes(128, 512, nvfp4.SWIZZLED)
+    for r0, r1 in zip(bounds[:-1], bounds[1:]):
+        part = gpu_run(x[r0:r1], x_dev=xd[r0:r1], amax=A, row0=r0, **kw)
+        assert np.array_equal(part["codes_row"], whole["codes_row"][r0:r1]), r0
+        assert np.array_equal(part["scales_row"], whole["scales_row"][r0 // 128 * cs_band:r1 // 128 * cs_band]), r0
+        assert same_float_bits(part["global_scale"], whole["global_scale"])
+
+
+@pytest.mark.parametrize("rht", [False, True])
+def test_column_shards_reproduce_the_whole_tensor(rht):
+    x = mixed_input(256, 1024, seed=22)
+    xd = to_device(x)
+    kw = dict(mode="sr", rht=rht, sign_mask=0x1357, seed=9, offset=4, rowwise=False, colwise=True)
+    whole = gpu_run(x, x_dev=xd, **kw)
+    A = torch.from_numpy(whole["amax"]).cuda()
+    for c0, c1 in [(0, 384), (384, 512), (512, 1024)]:
+        part = gpu_run(x[:, c0:c1].contiguous(), x_dev=xd[:, c0:c1], amax=A, col0=c0, **kw)
+        assert np.array_equal(part["codes_col"], whole["codes_col"][c0:c1]), c0
+        assert np.array_equal(part["scales_col"].reshape(c1 - c0, -1), whole["scales_col"].reshape(1024, -1)[c0:c1])
+
+
+def test_per_row_shards_need_no_exchange():
+    x = mixed_input(300, 256, seed=23)
+    xd = to_device(x)
+    kw = dict(mode="sr", per_row=True, seed=10)
+    whole = gpu_run(x, x_dev=xd, **kw)
+    for r0, r1 in [(0, 100), (100, 300)]:
+        part = gpu_run(x[r0:r1], x_dev=xd[r0:r1], row0=r0, **kw)
+        assert np.array_equal(part["codes_row"], whole["codes_row"][r0:r1])
+        assert np.array_equal(part["scales_row"].reshape(r1 - r0, -1), whole["scales_row"].reshape(300, -1)[r0:r1])
+        assert same_float_bits(part["amax"], whole["amax"][r0:r1])
