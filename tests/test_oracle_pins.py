@@ -235,6 +235,15 @@ def test_philox_matches_torch_header(torch_philox):
         assert oracle.philox4x32_10(ctr, key) == r, (seed, sub, off)
 
 
+def test_philox_known_answer_vectors():
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        v = [int(t, 16) for t in r]
+        assert oracle.philox4x32_10(v[0:4], v[4:6]) == v[6:10], r
+
+
 def test_sr_counter_layout(torch_philox):
     """Block (r, j) of the output draws Philox(key=seed, counter=(blk, offset)),
     blk = r * (C/16) + j, byte e&3 of word e>>2 for element e.
