@@ -131,10 +131,10 @@ typedef struct {
 } nvfp4_output;
 
 /* Workspace: per-tensor modes need a small device buffer for the amax
- * reduction (a running maximum, a CTA counter and a status word).  Allocate
- * nvfp4_workspace_bytes() bytes, zero them once before first use; every call
- * leaves them zero again.  Calls that share a workspace must not run
- * concurrently on the GPU. */
+ * reduction (a running maximum and a few counters).  Allocate
+ * nvfp4_workspace_bytes() bytes, 8-byte aligned, and zero them once before
+ * first use; every call leaves them zero again.  Calls that share a workspace
+ * must not run concurrently on the GPU. */
 size_t nvfp4_workspace_bytes(void);
 
 /* Bytes of one scale array for an [rows_out, cols_out] output (swizzle
@@ -177,7 +177,7 @@ nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16
  * nothing (no cudaMalloc, cudaFree or allocating library routine): the amax
  * pass's scratch lives in a 256-byte device array inside the library, which
  * every GPU that loads the library keeps until the process exits.  The pass
- * needs 12 of those bytes for any input size; the call returns
+ * needs 80 of those bytes for any input size; the call returns
  * NVFP4_ERR_UNSUPPORTED if the library's workspace need ever exceeds the array.
  * Inputs and outputs are as for nvfp4_quantize_rht_sr, whose checks (sizes
  * included) apply unchanged.

@@ -17,7 +17,7 @@ struct QArgs {
     uint8_t *codes_row, *scales_row, *codes_col, *scales_col;
     float *amax;          // per tensor: [1] (input to the quantize kernels); per row: [R_out]
     float *gscale;        // written: [1] or [R_out]
-    uint32_t *workspace;  // [0] running max bits, [1] CTA ticket, [2] status
+    uint32_t *workspace;  // [0] running max bits, [1] CTA count in, [2] CTA count out, [4..19] tile counters
     uint32_t sign_mask;
     uint64_t seed, offset;
     // Philox4x32-10 round keys of `seed` (key + round * Weyl constant),
@@ -55,12 +55,16 @@ cudaError_t launch_quant_col(const QArgs &a, bool fp32, int mode, bool rht, cuda
 cudaError_t launch_quant_2d(const QArgs &a, bool fp32, cudaStream_t s);
 // Rowwise with one global scale per row, amax and quantize in one pass.
 cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+// Per-tensor rowwise quantize including the amax pass, one cooperative launch
+// (an error return means nothing was enqueued).
+cudaError_t launch_quant_row_fused(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
 // The same launches with the fast-math element quotient (defined in their own
 // translation units).
 cudaError_t launch_quant_row_approx(const QArgs &a, bool fp32, int mode, bool rht, bool scaled_rows,
                                     cudaStream_t s);
 cudaError_t launch_quant_col_approx(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
 cudaError_t launch_quant_2d_approx(const QArgs &a, bool fp32, cudaStream_t s);
+cudaError_t launch_quant_row_fused_approx(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
 // Zero the pad bytes of a swizzled scale array.
 cudaError_t launch_scale_pad(uint8_t *scales, int64_t rows_out, int64_t cs, cudaStream_t s);
 

@@ -9,6 +9,11 @@ cudaError_t launch_quant_row(const QArgs &a, bool fp32, int mode, bool rht, cuda
                        : quant_row_launch<false>(a, fp32, mode, rht, false, s);
 }
 
+cudaError_t launch_quant_row_fused(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s) {
+    return a.fast_math ? launch_quant_row_fused_approx(a, fp32, mode, rht, s)
+                       : quant_row_fused_launch<false>(a, fp32, mode, rht, s);
+}
+
 cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s) {
     return a.fast_math ? launch_quant_row_approx(a, fp32, mode, rht, true, s)
                        : quant_row_launch<false>(a, fp32, mode, rht, true, s);

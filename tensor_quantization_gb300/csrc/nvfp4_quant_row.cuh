@@ -232,6 +232,262 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------------
+// Per-tensor rowwise quantize of a small tensor in one cooperative launch.
+//
+// Below a few million elements the amax pass and the quantize pass each cost
+// little more than a launch, so both run in one kernel: pass 1 streams the
+// CTA's tiles (TMA, kFusedStages in flight) and reduces its amax, a grid
+// barrier makes the tensor amax known to every CTA, and pass 2 streams the
+// same tiles again (from L2) and encodes them.  A tile is TR = 128 rows x 64
+// columns; thread t takes tile row t % 128 and blocks 2h, 2h+1 (h = t / 128).
+// Warps release a stage through an mbarrier (one arrival per warp) instead of
+// a CTA barrier, and thread 0 refills it once every warp has released it.
+// (Larger tensors run the amax and quantize kernels, whose second launch
+// overlaps the first's tail; there the one-kernel form gains nothing.)
+constexpr int kFusedThreads = 256;
+constexpr int kFusedTileRows = 128;
+constexpr int kFusedStages = 3;
+constexpr uint32_t kMaxGridPolls = 1u << 24;  // x >= 64 ns: the grid barrier gives up after ~1 s
+
+template <typename T>
+struct FusedTile {
+    static constexpr int kBoxCols = 128 / (int)sizeof(T);
+    static constexpr int kBoxes = kTileCols / kBoxCols;  // column boxes: 1 (bf16) or 2 (fp32)
+    static constexpr int kBoxBytes = kFusedTileRows * 128;
+    static constexpr int kStageBytes = kBoxes * kBoxBytes;
+    static constexpr int kSmemBytes = kFusedStages * kStageBytes + 1024;
+};
+
+template <typename T>
+__device__ __forceinline__ void fused_stage_block(const uint8_t *stage, int row, int b, RawBlock<T> &raw) {
+    constexpr int kChunks = (int)sizeof(T);
+    constexpr int kPerBoxRow = 8 / kChunks;
+    const uint8_t *base = stage + (b / kPerBoxRow) * FusedTile<T>::kBoxBytes + row * 128;
+#pragma unroll
+    for (int k = 0; k < kChunks; k++) {
+        const int c = (b % kPerBoxRow) * kChunks + k;
+        raw.w[k] = *reinterpret_cast<const uint4 *>(base + ((c ^ (row & 7)) << 4));
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void fused_issue(const CUtensorMap *map, uint8_t *stage, uint64_t *bar, uint32_t tr,
+                                            uint32_t tc) {
+    using FT = FusedTile<T>;
+    mbar_arrive_expect_tx(bar, FT::kStageBytes);
+#pragma unroll
+    for (int b = 0; b < FT::kBoxes; b++)
+        tma_load_2d(stage + b * FT::kBoxBytes, map, (int32_t)(tc * kTileCols + b * FT::kBoxCols),
+                    (int32_t)(tr * kFusedTileRows), bar);
+}
+
+// One arrival on a stage's release barrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Thread 0 of every CTA: fold the CTA maximum (magnitude bits) into the
+// tensor maximum (ws[0]), count the CTA in (ws[1], ordered after the maximum
+// by release semantics) and wait until every CTA is in; the maximum is final
+// then and is read together with the count in one 64-bit load.  A second
+// count (ws[2]) lets the last CTA out clear ws[0..2] for the next call.
+// Returns false if the wait gave up.
+__device__ __forceinline__ bool grid_amax_barrier(uint32_t *ws, uint32_t m, uint32_t nctas, uint32_t &total) {
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(ws), "r"(m) : "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws + 1) : "memory");
+    bool ok = false;
+    unsigned long long v = 0;
+    for (uint32_t i = 0; i < kMaxGridPolls; ++i) {
+        asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ws) : "memory");
+        if ((uint32_t)(v >> 32) >= nctas) {
+            ok = true;
+            break;
+        }
+        if (i >= 4096) __nanosleep(64);  // spin first: the last CTA usually arrives within microseconds
+    }
+    total = (uint32_t)v;
+    if (atomicAdd(ws + 2, 1u) == nctas - 1) {  // every CTA has read the maximum
+        ws[0] = 0u;
+        ws[1] = 0u;
+        ws[2] = 0u;
+    }
+    return ok;
+}
+
+// Every warp releases load L (stage L % kFusedStages) after reading it;
+// thread 0 then waits for all warps and, if `more`, refills the stage through
+// refill(stage index).
+template <typename F>
+__device__ __forceinline__ bool fused_release(uint64_t *empty, uint32_t L, int tid, bool more, F &&refill) {
+    const uint32_t s = L % kFusedStages;
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(&empty[s]);
+    bool ok = true;
+    if (tid == 0 && more) {
+        ok = mbar_wait(&empty[s], (L / kFusedStages) & 1u);
+        fence_async_shared();
+        refill(s);
+    }
+    return ok;
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+__global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_constant__ CUtensorMap tmap,
+                                                                  const QArgs a) {
+    constexpr int NT = kFusedThreads, TR = kFusedTileRows;
+    using FT = FusedTile<T>;
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ DivTable tab;
+    __shared__ RhtMult rm;
+    __shared__ __align__(8) uint64_t full[kFusedStages];
+    __shared__ __align__(8) uint64_t empty[kFusedStages];
+    __shared__ uint32_t red[NT / 32];
+    __shared__ float amax_sh;
+    uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
+    const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, CS = C >> 4, csp = (CS + 3) & ~3u;
+    const uint32_t ntc = (C + kTileCols - 1) / kTileCols, ntr = (R + TR - 1) / TR;
+    const uint32_t ntiles = ntc * ntr, G = gridDim.x;
+    const uint32_t nk = blockIdx.x < ntiles ? (ntiles - blockIdx.x + G - 1) / G : 0;  // my tiles
+    const int tid = threadIdx.x, warp = tid >> 5, trow = tid % TR, jb = (tid / TR) * 2;
+    // load L (0 <= L < 2 nk) is the CTA's tile L % nk: pass 1, then pass 2
+    auto issue = [&](uint32_t L) {
+        const uint32_t t = blockIdx.x + (L % nk) * G, s = L % kFusedStages;
+        fused_issue<T>(&tmap, stages + s * FT::kStageBytes, &full[s], t / ntc, t % ntc);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kFusedStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NT / 32);
+        }
+        mbar_init_fence();
+        for (uint32_t L = 0; L < 2 * nk && L < (uint32_t)kFusedStages; L++) issue(L);
+    }
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
+    __syncthreads();
+    bool ok = true;
+
+    // ---------------- pass 1: amax
+    float m = 0.0f;
+    for (uint32_t k = 0; k < nk; ++k) {
+        const uint32_t s = k % kFusedStages;
+        ok &= mbar_wait(&full[s], (k / kFusedStages) & 1u);
+        const uint8_t *stage = stages + s * FT::kStageBytes;
+#pragma unroll
+        for (int b = 0; b < 2; b++) {
+            RawBlock<T> raw;
+            fused_stage_block<T>(stage, trow, jb + b, raw);  // past the edge: zeros
+            f2 v[8];
+            unpack(raw, v);
+            if (RHT) fwht16(v);
+            m = absmax_nan(m, block_amax(v));
+        }
+        // pass 2's first loads follow pass 1's last ones without a break
+        ok &= fused_release(empty, k, tid, k + kFusedStages < 2 * nk, [&](uint32_t) { issue(k + kFusedStages); });
+    }
+
+    // ---------------- grid-wide amax
+    {
+        uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m) & 0x7FFFFFFFu);
+        if ((tid & 31) == 0) red[warp] = mb;
+        __syncthreads();
+        if (tid < 32) {
+            mb = __reduce_max_sync(0xFFFFFFFFu, tid < NT / 32 ? red[tid] : 0u);
+            if (tid == 0) {
+                uint32_t bits = 0;
+                if (!grid_amax_barrier(a.workspace, mb, G, bits)) {
+                    atomicAdd(&g_wait_timeouts, 1u);
+                    ok = false;
+                }
+                float A = __uint_as_float(bits);
+                if (RHT) A = __fmul_rn(A, 0.25f);
+                amax_sh = A;
+                if (blockIdx.x == 0) {
+                    a.amax[0] = A;
+                    a.gscale[0] = global_scale_of(A);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const float g = global_scale_of(amax_sh);
+    build_table(tab, g, tid, blockDim.x);
+    const ScaleDiv sd = make_scale_div(g);
+    const bool fast = scale_all_fast(g);
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
+    __syncthreads();
+
+    // ---------------- pass 2: encode
+    const bool vec = (reinterpret_cast<uintptr_t>(a.codes_row) & 15u) == 0 && ((C >> 1) & 15u) == 0;
+    const bool svec = (reinterpret_cast<uintptr_t>(a.scales_row) & 1u) == 0;
+    const bool lin_svec = svec && (CS & 1u) == 0;
+    for (uint32_t k = 0; k < nk; ++k) {
+        const uint32_t L = nk + k, s = L % kFusedStages;
+        const uint32_t t = blockIdx.x + k * G;
+        ok &= mbar_wait(&full[s], (L / kFusedStages) & 1u);
+        const uint32_t tr = t / ntc, tc = t - tr * ntc;
+        const uint32_t row = tr * TR + trow, j0 = tc * 4 + jb;
+        const uint8_t *stage = stages + s * FT::kStageBytes;
+        if (row < R && j0 < CS) {
+            uint4 w[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            if (MODE == MODE_SR) {
+#pragma unroll
+                for (int b = 0; b < 2; b++) {
+                    const uint64_t blk = a.blk_base + (uint64_t)row * CS + j0 + b;
+                    w[b] = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
+                                               (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
+                }
+            }
+            uint32_t S[2] = {0u, 0u};
+            uint2 c[2];
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                RawBlock<T> raw;
+                fused_stage_block<T>(stage, trow, jb + b, raw);
+                f2 v[8];
+                unpack(raw, v);
+                if (fast) {
+                    c[b] = encode_block_fast<MODE, RHT, AP>(v, sd, tab, signs, w[b], S[b]);
+                } else {
+                    if (RHT) rht16(v, rm);
+                    c[b] = encode_block<MODE>(v, sd, tab, w[b], S[b]);
+                }
+            }
+            // the tile's blocks past the edge (j0 + b >= CS) are not stored;
+            // 16-byte stores need C % 32 == 0, so CS is even and j0 + 1 < CS
+            uint8_t *codes = a.codes_row + (int64_t)row * (C >> 1) + j0 * 8;
+            if (vec) {
+                *reinterpret_cast<uint4 *>(codes) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+            } else {
+                reinterpret_cast<uint2 *>(codes)[0] = c[0];
+                if (j0 + 1 < CS) reinterpret_cast<uint2 *>(codes)[1] = c[1];
+            }
+            if (a.swizzled) {  // j0 is even: the pair is contiguous in its 4-byte group (pad bytes 0)
+                uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+                if (svec) {
+                    *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(S[0] | (S[1] << 8));
+                } else {
+                    dst[0] = (uint8_t)S[0];
+                    dst[1] = (uint8_t)S[1];
+                }
+            } else {
+                uint8_t *dst = a.scales_row + (size_t)row * CS + j0;
+                if (lin_svec && j0 + 1 < CS) {
+                    *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(S[0] | (S[1] << 8));
+                } else {
+                    dst[0] = (uint8_t)S[0];
+                    if (j0 + 1 < CS) dst[1] = (uint8_t)S[1];
+                }
+            }
+        }
+        ok &= fused_release(empty, L, tid, L + kFusedStages < 2 * nk, [&](uint32_t) { issue(L + kFusedStages); });
+    }
+    if (!ok) {  // a bounded wait gave up somewhere in this CTA: the output is not trustworthy
+        atomicAdd(&g_wait_timeouts, 1u);
+        a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
+    }
+}
+
 template <int MODE, bool RHT, typename T>
 __global__ void __launch_bounds__(256) k_quant_rowscaled(const QArgs a) {
     __shared__ DivTable tab;
@@ -543,6 +799,54 @@ cudaError_t dispatch_row(const QArgs &a, int mode, bool rht, bool scaled_rows, c
     if (mode == MODE_SR) return rht ? run_row<MODE_SR, true, T, AP>(a, s) : run_row<MODE_SR, false, T, AP>(a, s);
     if constexpr (!AP) return run_row<MODE_4O6, false, T, false>(a, s);
     return cudaErrorInvalidValue;
+}
+
+template <int MODE, bool RHT, typename T, bool AP>
+cudaError_t run_row_fused(const QArgs &a, cudaStream_t s) {
+    auto k = k_quant_row_fused<MODE, RHT, T, AP>;
+    constexpr int smem = FusedTile<T>::kSmemBytes;
+    static bool configured = false;  // one attribute call per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kFusedThreads, smem) != cudaSuccess || per_sm < 1)
+        return cudaErrorNotSupported;
+    CUtensorMap map;
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, FusedTile<T>::kBoxCols, kFusedTileRows))
+        return cudaErrorInvalidValue;
+    const int64_t tiles = ((a.rows + kFusedTileRows - 1) / kFusedTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, map, a);
+}
+
+template <typename T, bool AP>
+cudaError_t dispatch_row_fused(const QArgs &a, int mode, bool rht, cudaStream_t s) {
+    if (mode == MODE_RNE) return rht ? run_row_fused<MODE_RNE, true, T, AP>(a, s) : run_row_fused<MODE_RNE, false, T, AP>(a, s);
+    if (mode == MODE_SR) return rht ? run_row_fused<MODE_SR, true, T, AP>(a, s) : run_row_fused<MODE_SR, false, T, AP>(a, s);
+    if constexpr (!AP) return run_row_fused<MODE_4O6, false, T, false>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+// Per-tensor rowwise quantize with the amax pass folded in (one cooperative
+// launch).  Returns an error without enqueuing anything if the launch is not
+// possible; the caller then runs the amax and quantize kernels instead.
+template <bool AP>
+cudaError_t quant_row_fused_launch(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s) {
+    return fp32 ? dispatch_row_fused<float, AP>(a, mode, rht, s) : dispatch_row_fused<bf16_t, AP>(a, mode, rht, s);
 }
 
 // Rowwise launches of one quotient kind (AP: fast math).

@@ -10,4 +10,8 @@ cudaError_t launch_quant_row_approx(const QArgs &a, bool fp32, int mode, bool rh
     return quant_row_launch<true>(a, fp32, mode, rht, scaled_rows, s);
 }
 
+cudaError_t launch_quant_row_fused_approx(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s) {
+    return quant_row_fused_launch<true>(a, fp32, mode, rht, s);
+}
+
 }  // namespace nvfp4

@@ -485,3 +485,54 @@ def test_per_row_shards_need_no_exchange():
         assert np.array_equal(part["codes_row"], whole["codes_row"][r0:r1])
         assert np.array_equal(part["scales_row"].reshape(r1 - r0, -1), whole["scales_row"].reshape(300, -1)[r0:r1])
         assert same_float_bits(part["amax"], whole["amax"][r0:r1])
+
+
+# ------------------------------------------------- which kernels a call runs
+def _kernels_of(fn) -> list[str]:
+    """Names of the CUDA kernels launched by fn() (CUPTI through torch.profiler)."""
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    return [n for n in names if "nvfp4" in n or n.startswith(("k_", "void nvfp4", "nvfp4"))]
+
+
+@pytest.mark.parametrize("case", ["row_rht_sr_bf16", "row_rht_sr_fp32", "row_rne", "row_4o6", "col_rht_sr",
+                                  "row_large"])
+def test_per_tensor_call_launches(case):
+    """A small per-tensor rowwise call is one cooperative kernel (amax pass
+    folded in); a large one, or a columnwise one, is the amax kernel and the
+    quantize kernel."""
+    dtype = torch.float32 if case.endswith("fp32") else torch.bfloat16
+    shape = (4096, 2048) if case == "row_large" else (1024, 2048)
+    x = to_device(mixed_input(*shape, seed=24, dtype=dtype))
+    kw = {"row_rht_sr_bf16": dict(mode="sr", rht=True, sign_mask=3, seed=1, swizzled=True),
+          "row_rht_sr_fp32": dict(mode="sr", rht=True, sign_mask=3, seed=1, swizzled=True),
+          "row_rne": dict(mode="rne"), "row_4o6": dict(mode="4o6"),
+          "col_rht_sr": dict(mode="sr", rht=True, rowwise=False, colwise=True, seed=2),
+          "row_large": dict(mode="sr", rht=True, sign_mask=3, seed=1)}[case]
+    nvfp4.quantize(x, **kw)  # first call configures the kernels
+    names = _kernels_of(lambda: nvfp4.quantize(x, **kw))
+    if not names:
+        pytest.skip("no kernel activity recorded (CUPTI unavailable)")
+    if case == "row_large":
+        assert len(names) == 2 and "k_amax" in names[0] and "k_quant_row" in names[1], names
+    elif case.startswith("row"):
+        assert len(names) == 1 and "k_quant_row_fused" in names[0], names
+    else:
+        assert len(names) == 2 and "k_amax" in names[0] and "k_quant_col" in names[1], names
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_two_kernel_rowwise_path_ragged(mode, dtype):
+    """Per-tensor rowwise tensors above the one-kernel size limit run the amax
+    kernel and the TMA quantize kernel: a shape with ragged row and column
+    tiles (2100 rows, 129 blocks per row) against the oracle."""
+    rows, cols = 2112 if dtype == torch.float32 else 2100, 2064
+    x = mixed_input(rows, cols, seed=25, dtype=dtype)
+    kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", swizzled=True, sign_mask=0x2222,
+              seed=12, offset=1)
+    assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
