@@ -215,7 +215,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     def flush_l2(k: int) -> None:
         flush.fill_(k & 0xFF)  # evicts everything
         scrub.max()  # write-back of the dirty flush lines happens here, untimed
-    split = not w.per_row  # per-tensor: amax pass then encode, timed separately
+    amax_kernel, quant_kernel = kernel_plan(w)
+    split = amax_kernel is not None  # two kernels: amax pass then encode, also timed separately
 
     def quant_call(fl):
         if w.mode == "sr" and w.rht:
@@ -266,15 +267,20 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     total_ms = max_over_ranks(sum(step_ms), world, dev)
 
     # per-kernel durations: the same steps issued as two calls with an event
-    # between the passes (same kernels; the event keeps them from overlapping)
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush_l2(k)
-        step(*sevs[k])
-    torch.cuda.synchronize(dev)
-    k1_ms = [e[0].elapsed_time(e[1]) for e in sevs]
-    k2_ms = [e[1].elapsed_time(e[2]) for e in sevs]
-    split_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in sevs)
+    # between the passes (same kernels; the event keeps them from overlapping).
+    # A one-kernel call is its own kernel duration.
+    if split:
+        sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush_l2(k)
+            step(*sevs[k])
+        torch.cuda.synchronize(dev)
+        k1_ms = [e[0].elapsed_time(e[1]) for e in sevs]
+        k2_ms = [e[1].elapsed_time(e[2]) for e in sevs]
+        split_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in sevs)
+    else:
+        k1_ms, k2_ms = [0.0], step_ms
+        split_ms = statistics.mean(step_ms)
 
     # end to end through the public API: pinned host input -> device, the
     # fused call (amax pass + encode), codes/scales/scale words -> pinned host
@@ -304,10 +310,14 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     peak, peak_src = hbm_peak()
     k1, k2 = statistics.mean(k1_ms), statistics.mean(k2_ms)
     if split and k1 > k2:
-        dom, dom_bytes, dom_ms, unit_desc = "k_amax", nbytes["amax_pass"], k1, "2 B read per element"
-    else:
-        dom, dom_bytes, dom_ms = "k_quant", nbytes["quantize"], k2
+        dom, dom_bytes, dom_ms, unit_desc = amax_kernel, nbytes["amax_pass"], k1, "2 B read per element"
+    elif split:
+        dom, dom_bytes, dom_ms = quant_kernel, nbytes["quantize"], k2
         unit_desc = "2 B read + 0.5 B codes + 1/16 B scale per element (+ scale words)"
+    else:
+        dom, dom_bytes, dom_ms = quant_kernel, nbytes["total"], k2
+        unit_desc = ("2 B read + 0.5 B codes + 1/16 B scale per element + 8 B of scale words per row" if w.per_row
+                     else "2 B read twice (amax pass, encode) + 0.5 B codes + 1/16 B scale per element")
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = profile_traffic(dom, w.name)
     hbm_view = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -316,7 +326,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": dom_bytes,
                 "per_unit": unit_desc, "ms_per_launch": round(dom_ms, 5)}
     roofline = hbm_view
-    wipe = profile_field(dom, w.name, "warp_inst_per_element") if dom == "k_quant" else None
+    wipe = profile_field(dom, w.name, "warp_inst_per_element")
     if wipe:
         # the quantize kernel reads its input from L2 and is issue-bound: its
         # roofline is the issue rate, 1 warp instruction per cycle per scheduler
@@ -329,8 +339,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
                     "unit": "Gwarp-inst/s", "frac": round(ach_i / peak_i, 4), "traffic": traffic,
                     "peak_source": f"{sms} SMs x 4 schedulers x 1 warp-instruction/cycle x {mhz:.0f} MHz max SM clock",
                     "instructions_per_launch": round(inst),
-                    "instructions_source": "ncu smsp__inst_executed.sum per element, profiles/k_quant__"
-                                           + w.name + ".md",
+                    "instructions_source": f"ncu smsp__inst_executed.sum per element, profiles/{dom}__{w.name}.md",
                     "ms_per_launch": round(dom_ms, 5), "hbm_view": {k: hbm_view[k] for k in
                                                                      ("achieved", "peak", "unit", "frac")}}
     res = {
@@ -344,12 +353,14 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         "counted_bytes_per_step": nbytes["total"],
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": roofline,
-        "kernels_ms": {"k_amax": round(k1, 5) if split else None, "k_quant": round(k2, 5),
-                       "split_step": round(split_ms, 5), "source": "second loop, event between the passes"},
+        "kernels_ms": ({amax_kernel: round(k1, 5), quant_kernel: round(k2, 5), "split_step": round(split_ms, 5),
+                        "source": "second loop, event between the passes"} if split else
+                       {quant_kernel: round(k2, 5), "source": "the timed steps (one kernel per call)"}),
         "e2e": {"value": round(nbytes["total"] / (statistics.mean(e2e_ms) * 1e-3) / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(statistics.mean(e2e_ms), 4)},
         "gpu_launches": args.steps * (2 if split else 1) + (args.steps if pad_launch_needed(w) else 0),
+        "kernels": [k for k in (amax_kernel, quant_kernel) if k],
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
@@ -362,6 +373,29 @@ def workload_of(args) -> wl.Workload:
         r, c = (int(v) for v in args.shape.lower().split("x"))
         w = w.resized(r, c)
     return w
+
+
+FUSED_MAX_ELEMS = 1 << 22  # the library's one-kernel limit for per-tensor rowwise calls
+ROWSCALED_STAGED_MAX_ROW_BYTES = 96 * 1024
+
+
+def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
+    """(amax kernel or None, quantize kernel) that one call of this workload
+    launches, by the library's dispatch rules."""
+    if w.per_row:
+        return None, ("k_quant_rowscaled_staged" if w.cols * 2 <= ROWSCALED_STAGED_MAX_ROW_BYTES
+                      else "k_quant_rowscaled")
+    if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
+        return None, "k_quant_row_fused"
+    if not w.rht:
+        amax = "k_amax_plain"
+    else:
+        amax = "k_amax_rht_col" if (w.colwise and not w.rowwise) else "k_amax_rht_row"
+    if w.block2d:
+        return amax, "k_quant_2d"
+    if w.colwise and not w.rowwise:
+        return amax, "k_quant_col"
+    return amax, "k_quant_row"
 
 
 def pad_launch_needed(w: wl.Workload) -> bool:

@@ -17,7 +17,7 @@ struct QArgs {
     uint8_t *codes_row, *scales_row, *codes_col, *scales_col;
     float *amax;          // per tensor: [1] (input to the quantize kernels); per row: [R_out]
     float *gscale;        // written: [1] or [R_out]
-    uint32_t *workspace;  // [0] running max bits, [1] CTA count in, [2] CTA count out, [4..19] tile counters
+    uint32_t *workspace;  // [0] running max bits, [1] CTA count (in), [2] CTA count (out)
     uint32_t sign_mask;
     uint64_t seed, offset;
     // Philox4x32-10 round keys of `seed` (key + round * Weyl constant),
