@@ -38,21 +38,35 @@ __device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, 
     }
 }
 
-// No RHT: the maximum over every element, any orientation.
+// No RHT: the maximum over every element, any orientation.  A thread takes
+// kPlainUnroll 16-byte chunks per step (all loads issued before any is
+// used), so enough bytes are in flight to stream at HBM rate.
+constexpr int kPlainUnroll = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(256) k_amax_plain(const QArgs a) {
     constexpr int W = Chunk<T>::W;
     const uint32_t NCH = (uint32_t)((a.cols + W - 1) / W);
     const uint32_t n = (uint32_t)a.rows * NCH;
     const T *x = static_cast<const T *>(a.x);
+    const uint32_t stride = gridDim.x * blockDim.x;
     uint32_t m = 0;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const uint32_t r = i / NCH, ch = i - r * NCH;
-        const int64_t c0 = (int64_t)ch * W;
-        Chunk<T> c;
-        c.load(x + (int64_t)r * a.ld + c0, (int)min((int64_t)W, a.cols - c0));
+    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += kPlainUnroll * stride) {
+        Chunk<T> c[kPlainUnroll];
 #pragma unroll
-        for (int e = 0; e < W; e++) m = max(m, mag_bits(c.get(e)));
+        for (int u = 0; u < kPlainUnroll; u++) {
+            const uint32_t i = i0 + u * stride;
+            if (i < n) {
+                const uint32_t r = i / NCH, ch = i - r * NCH;
+                const int64_t c0 = (int64_t)ch * W;
+                c[u].load(x + (int64_t)r * a.ld + c0, (int)min((int64_t)W, a.cols - c0));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPlainUnroll; u++)
+            if (i0 + u * stride < n)
+#pragma unroll
+                for (int e = 0; e < W; e++) m = max(m, mag_bits(c[u].get(e)));
     }
     publish_tensor_amax(a, m, false);
 }
