@@ -126,7 +126,8 @@ typedef struct {
 typedef struct {
     uint8_t *codes_row, *scales_row;
     uint8_t *codes_col, *scales_col;
-    float *amax;         /* 1 float, or R_out floats with NVFP4_SCALE_PER_ROW */
+    float *amax;         /* 1 float, R_out floats with NVFP4_SCALE_PER_ROW, or 2
+                            with the RHT in both orientations                 */
     float *global_scale; /* same count as amax; written by every call         */
 } nvfp4_output;
 
@@ -164,7 +165,12 @@ nvfp4_status nvfp4_quantize_sr(const nvfp4_input *in, uint32_t flags, uint64_t s
                                nvfp4_output *out, void *workspace, void *stream);
 
 /* 16-point RHT (sign_mask bit j = 1 negates output j of each block) followed
- * by stochastic rounding, as nvfp4_quantize_sr.  Exactly one orientation. */
+ * by stochastic rounding, as nvfp4_quantize_sr.  Either orientation, or both
+ * from one call (the operand of a weight-gradient GEMM needs both): the
+ * transform then runs along the rows for the rowwise output and along the
+ * columns for the columnwise one, the two amaxes differ, and out->amax and
+ * out->global_scale hold two floats, [0] rowwise and [1] columnwise (with
+ * NVFP4_AMAX_GIVEN both are read). */
 nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16_t sign_mask,
                                    uint64_t seed, uint64_t offset, nvfp4_output *out,
                                    void *workspace, void *stream);

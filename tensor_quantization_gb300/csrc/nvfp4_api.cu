@@ -84,7 +84,6 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
     if (!want_row && !want_col) return NVFP4_ERR_INVALID_ARG;
     if (block2d && (mode != nvfp4::MODE_RNE_ID || rht || per_row)) return NVFP4_ERR_UNSUPPORTED;
     if (per_row && (want_col || given)) return NVFP4_ERR_UNSUPPORTED;
-    if (rht && want_row && want_col) return NVFP4_ERR_UNSUPPORTED;
     if (rht && mode == nvfp4::MODE_4O6_ID) return NVFP4_ERR_UNSUPPORTED;
     if ((flags & NVFP4_FAST_MATH) && mode == nvfp4::MODE_4O6_ID) return NVFP4_ERR_UNSUPPORTED;
     // a stochastic shard is cut along its output rows only
@@ -98,7 +97,10 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
         return NVFP4_ERR_INVALID_ARG;
     if (!empty && want_col && (!out->codes_col || !out->scales_col || !aligned(out->codes_col, 8)))
         return NVFP4_ERR_INVALID_ARG;
-    const int64_t n_scale = per_row ? in->rows : 1;
+    // per row: one scale per row; RHT in both orientations: one per orientation
+    // (the transform runs along different axes, so the two amaxes differ)
+    const bool two_scales = rht && want_row && want_col;
+    const int64_t n_scale = per_row ? in->rows : (two_scales ? 2 : 1);
     if (n_scale > 0 && (!out->amax || !out->global_scale)) return NVFP4_ERR_INVALID_ARG;
     if (!per_row && !given && !empty && (!ws || !aligned(ws, 8))) return NVFP4_ERR_INVALID_ARG;
 
@@ -136,12 +138,23 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
     } else if (per_row) {
         st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, mode, rht, s));
     } else {
-        if (!given) {
-            st = cuda_status(nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col, s));
+        if (!given) {  // (both orientations with the RHT: the rowwise amax first)
+            st = cuda_status(nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col && !want_row, s));
             if (st != NVFP4_OK) return st;
         }
         if (block2d) {
             st = cuda_status(nvfp4::launch_quant_2d(a, fp32, s));
+        } else if (two_scales) {
+            // rowwise with amax[0] / global_scale[0], then columnwise with [1]
+            nvfp4::QArgs ar = a, ac = a;
+            ar.want_col = 0;
+            ac.want_row = 0;
+            ac.amax = out->amax + 1;
+            ac.gscale = out->global_scale + 1;
+            ac.blk_base = base_col;
+            st = cuda_status(nvfp4::launch_quant_row(ar, fp32, mode, rht, s));
+            if (st == NVFP4_OK && !given) st = cuda_status(nvfp4::launch_amax_tensor(ac, fp32, rht, true, s));
+            if (st == NVFP4_OK) st = cuda_status(nvfp4::launch_quant_col(ac, fp32, mode, rht, s));
         } else {
             if (want_row) st = cuda_status(nvfp4::launch_quant_row(a, fp32, mode, rht, s));
             if (st == NVFP4_OK && want_col) {
@@ -211,7 +224,6 @@ nvfp4_status nvfp4_quantize_sr(const nvfp4_input *in, uint32_t flags, uint64_t s
 
 nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16_t sign_mask, uint64_t seed,
                                    uint64_t offset, nvfp4_output *out, void *workspace, void *stream) {
-    if ((flags & NVFP4_ROWWISE) && (flags & NVFP4_COLWISE)) return NVFP4_ERR_UNSUPPORTED;
     return quantize(in, flags, nvfp4::MODE_SR_ID, true, sign_mask, seed, offset, out, workspace, stream);
 }
 

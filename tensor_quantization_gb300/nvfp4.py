@@ -213,7 +213,9 @@ class Workspace:
         return ws
 
 
-def alloc_outputs(x: torch.Tensor, flags: int) -> Quantized:
+def alloc_outputs(x: torch.Tensor, flags: int, rht: bool = False) -> Quantized:
+    """Device outputs for `flags`; with the RHT in both orientations the amax
+    and global scale hold two floats ([0] rowwise, [1] columnwise)."""
     R, C = x.shape
     dev = x.device
     cr = sr = cc = sc = None
@@ -223,7 +225,7 @@ def alloc_outputs(x: torch.Tensor, flags: int) -> Quantized:
     if flags & COLWISE:
         cc = torch.empty(C, R // 2, dtype=torch.uint8, device=dev)
         sc = torch.empty(nvfp4_scale_bytes(C, R, flags), dtype=torch.uint8, device=dev)
-    n = R if flags & SCALE_PER_ROW else 1
+    n = R if flags & SCALE_PER_ROW else (2 if rht and flags & ROWWISE and flags & COLWISE else 1)
     amax = torch.empty(n, dtype=torch.float32, device=dev)
     gs = torch.empty(n, dtype=torch.float32, device=dev)
     return Quantized(cr, sr, cc, sc, amax, gs, flags)
@@ -237,7 +239,7 @@ def quantize(x: torch.Tensor, *, mode: str = "rne", rowwise: bool = True, colwis
     flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (BLOCK_2D if block2d else 0) | \
         (SCALE_PER_ROW if per_row else 0) | (SWIZZLED if swizzled else 0) | \
         (AMAX_GIVEN if amax is not None else 0) | (FAST_MATH if fast_math else 0)
-    q = out if out is not None else alloc_outputs(x, flags)
+    q = out if out is not None else alloc_outputs(x, flags, rht)
     if amax is not None:
         q.amax.copy_(amax)
     o = make_output(q.codes_row, q.scales_row, q.codes_col, q.scales_col, q.amax, q.global_scale)

@@ -72,7 +72,10 @@ def test_arguments_are_rejected_before_any_launch(lib):
     assert st(ctypes.byref(_inp(16, 32, 32)), 3 | nvfp4.SCALE_PER_ROW, ctypes.byref(out), ws, None) == \
         nvfp4.ERR_UNSUPPORTED
     rht = lib.nvfp4_quantize_rht_sr
-    assert rht(ctypes.byref(_inp(16, 32, 32)), 3, 0, 1, 0, ctypes.byref(out), ws, None) == nvfp4.ERR_UNSUPPORTED
+    assert rht(ctypes.byref(_inp(16, 32, 32)), 1 | nvfp4.BLOCK_2D, 0, 1, 0, ctypes.byref(out), ws, None) == \
+        nvfp4.ERR_UNSUPPORTED
+    assert rht(ctypes.byref(_inp(16, 32, 32)), 3 | nvfp4.SCALE_PER_ROW, 0, 1, 0, ctypes.byref(out), ws, None) == \
+        nvfp4.ERR_UNSUPPORTED
     fo6 = lib.nvfp4_quantize_four_over_six
     assert fo6(ctypes.byref(_inp(16, 32, 32)), 1 | nvfp4.FAST_MATH, ctypes.byref(out), ws, None) == \
         nvfp4.ERR_UNSUPPORTED

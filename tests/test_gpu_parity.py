@@ -71,15 +71,24 @@ def oracle_run(x_cpu: torch.Tensor, *, mode="rne", rowwise=True, colwise=False, 
     xn = np_bits(x_cpu)
     kw = dict(mode=mode, block2d=block2d, per_row=per_row, swizzled=swizzled, rht=rht, sign_mask=sign_mask,
               seed=seed, offset=offset, row_range=row_range,
-              amax_given=None if amax is None else float(amax))
+              amax_given=None if amax is None else float(np.asarray(amax).ravel()[0]))
     out = {}
+    amaxes, scales = [], []
     for orient, on in (("row", rowwise), ("col", colwise)):
         if not on:
             continue
-        o = oracle.quantize(xn, colwise=(orient == "col"), **kw)
+        okw = dict(kw)
+        if rht and rowwise and colwise and amax is not None:  # two given amaxes: [0] rows, [1] columns
+            okw["amax_given"] = float(np.asarray(amax).ravel()[0 if orient == "row" else 1])
+        o = oracle.quantize(xn, colwise=(orient == "col"), **okw)
         out[f"codes_{orient}"] = o["codes"]
         out[f"scales_{orient}"] = o["scales"].ravel()
-        out["amax"], out["global_scale"] = o["amax"], o["global_scale"]
+        amaxes.append(o["amax"])
+        scales.append(o["global_scale"])
+    if rht and rowwise and colwise:  # one amax per orientation
+        out["amax"], out["global_scale"] = np.concatenate(amaxes), np.concatenate(scales)
+    else:
+        out["amax"], out["global_scale"] = amaxes[-1], scales[-1]
     return out
 
 
@@ -185,8 +194,6 @@ MODES = ["rne", "sr", "rht_sr", "4o6"]
 @pytest.mark.parametrize("orient", ["row", "col", "both"])
 @pytest.mark.parametrize("mode", MODES)
 def test_option_matrix(mode, orient, swizzled, dtype):
-    if mode == "rht_sr" and orient == "both":
-        pytest.skip("the RHT path takes one orientation per call")
     x = mixed_input(160, 208, seed=zlib.crc32(f"{mode}{orient}{swizzled}{dtype}".encode()) & 0xFFFF, dtype=dtype)
     kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", rowwise=orient in ("row", "both"),
               colwise=orient in ("col", "both"), swizzled=swizzled, sign_mask=0xB4E1, seed=77, offset=5)
@@ -307,6 +314,22 @@ def test_strided_input_rows():
     for kw in (dict(mode="rne"), dict(mode="sr", rht=True, seed=8), dict(mode="rne", colwise=True),
                dict(mode="4o6", per_row=True), dict(mode="rne", block2d=True, colwise=True)):
         assert_parity(gpu_run(x_cpu, x_dev=x_dev, **kw), oracle_run(x_cpu, **kw))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("swizzled", [False, True], ids=["linear", "swizzled"])
+def test_rht_both_orientations_from_one_call(swizzled, dtype):
+    """RHT + SR into both orientations: each orientation transforms along its own
+    blocks and has its own amax ([0] rowwise, [1] columnwise)."""
+    x = mixed_input(272, 208, seed=26, dtype=dtype)
+    kw = dict(mode="sr", rht=True, rowwise=True, colwise=True, swizzled=swizzled, sign_mask=0x3C5A, seed=13,
+              offset=2)
+    g, o = gpu_run(x, **kw), oracle_run(x, **kw)
+    assert g["amax"].shape == (2,) and g["amax"][0] != g["amax"][1]
+    assert_parity(g, o)
+    # the same with both amaxes given
+    A = torch.from_numpy(o["amax"] * np.float32(1.5)).cuda()
+    assert_parity(gpu_run(x, amax=A, **kw), oracle_run(x, amax=A.cpu().numpy(), **kw))
 
 
 def test_amax_given():
