@@ -203,6 +203,28 @@ nvfp4_status nvfp4_quantize_rht_sr_static(const nvfp4_input *in, uint32_t flags,
 nvfp4_status nvfp4_quantize_four_over_six(const nvfp4_input *in, uint32_t flags, nvfp4_output *out,
                                           void *workspace, void *stream);
 
+/* Grouped rowwise quantize: many tensors in one call, e.g. the tokens routed
+ * to each expert of a mixture-of-experts layer, stacked as the row ranges of
+ * one input ("[nvfp4 training][rl] Add a CuTe DSL fast-path kernel for
+ * four-over-six quantize #4852", PR description: grouped / MoE quantization is
+ * the named follow-up).  group_offsets is a DEVICE array of n_groups+1
+ * non-decreasing row indices, group_offsets[0] = 0 and group_offsets[n_groups]
+ * = rows; group g is rows [group_offsets[g], group_offsets[g+1]) (it may be
+ * empty) and is quantized as a tensor of its own: its own amax and global
+ * scale (out->amax and out->global_scale hold n_groups floats; an empty group
+ * gets 0), with the block scales and codes written into the rows of the one
+ * output.  Philox blocks keep their numbers in the whole input.  mode: one of
+ * NVFP4_MODE_*.  flags: NVFP4_ROWWISE (required), NVFP4_SWIZZLED,
+ * NVFP4_AMAX_GIVEN (out->amax holds the n_groups amaxes).  Rows are staged in
+ * shared memory: cols * element size <= 96 KiB, else NVFP4_ERR_UNSUPPORTED.
+ * Needs no workspace.  Launches an amax kernel, a tiny finalising kernel and
+ * the per-row-scale quantize kernel (which takes each row's scale from its
+ * group). */
+enum { NVFP4_MODE_RNE = 0, NVFP4_MODE_SR = 1, NVFP4_MODE_RHT_SR = 2, NVFP4_MODE_FOUR_OVER_SIX = 3 };
+nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const int64_t *group_offsets,
+                                    int64_t n_groups, int32_t mode, uint16_t sign_mask, uint64_t seed,
+                                    uint64_t offset, nvfp4_output *out, void *stream);
+
 /* Standard NVFP4 decode: out[r][c] = value(code) * (Sf * g), both products
  * rounded to fp32 (then to bf16 for a bf16 output).  codes [rows, cols/2],
  * scales linear or swizzled per flags (NVFP4_SWIZZLED), global_scale 1 float or

@@ -161,6 +161,57 @@ __global__ void __launch_bounds__(256) k_amax_rows(const QArgs a) {
     }
 }
 
+// Grouped rowwise scaling: n_groups row ranges, each its own tensor for the
+// amax.  A CTA takes a contiguous range of rows and, for each group segment in
+// it, reduces the segment's blocks (post-RHT magnitudes without the 0.25) and
+// folds the result into amax[g] with one atomicMax on its bits (the caller
+// zeroed amax[]; magnitude bits order like the floats, NaN above +inf).
+template <bool RHT, typename T>
+__global__ void __launch_bounds__(256) k_amax_groups(const QArgs a) {
+    __shared__ uint32_t red[32];
+    const uint32_t CS = (uint32_t)(a.cols >> 4);
+    const T *x = static_cast<const T *>(a.x);
+    const int64_t per = (a.rows + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = (int64_t)blockIdx.x * per, r1 = min(a.rows, r0 + per);
+    if (r0 >= r1) return;
+    // the group of r0: largest g with offsets[g] <= r0
+    int64_t lo = 0, hi = a.n_groups - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.group_offsets + mid) <= r0) lo = mid;
+        else hi = mid - 1;
+    }
+    uint32_t *bits = reinterpret_cast<uint32_t *>(a.amax);
+    for (int64_t g = lo; g < a.n_groups; ++g) {
+        const int64_t s0 = max(r0, __ldg(a.group_offsets + g)), s1 = min(r1, __ldg(a.group_offsets + g + 1));
+        if (s0 >= r1) break;
+        if (s0 >= s1) continue;  // an empty group, or one that ends before this range
+        const uint64_t nb = (uint64_t)(s1 - s0) * CS;
+        uint32_t m = 0;
+        for (uint64_t i = threadIdx.x; i < nb; i += blockDim.x) {
+            const int64_t r = s0 + (int64_t)(i / CS);
+            const uint32_t j = (uint32_t)(i % CS);
+            f2 v[8];
+            load_block_row(x + r * a.ld + 16 * j, v);
+            if (RHT) fwht16(v);
+            m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+        }
+        m = block_max_u32(m, red);
+        if (threadIdx.x == 0) atomicMax(bits + g, m);
+    }
+}
+
+// amax[g] from its bits (x 0.25 for the RHT, unless the caller gave it) and
+// global_scale[g] = amax[g] / 2688.
+__global__ void k_group_finalize(const QArgs a, int rht, int given) {
+    const int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (g >= a.n_groups) return;
+    float A = a.amax[g];
+    if (!given && rht) A = __fmul_rn(A, 0.25f);
+    a.amax[g] = A;
+    a.gscale[g] = global_scale_of(A);
+}
+
 template <typename K>
 static int grid_for(K kernel, int64_t work_items) {
     int per_sm = 0;
@@ -204,6 +255,27 @@ static cudaError_t run_amax_rows(const QArgs &a, cudaStream_t s) {
 cudaError_t launch_amax_rows(const QArgs &a, bool fp32, bool rht, cudaStream_t s) {
     if (fp32) return rht ? run_amax_rows<true, float>(a, s) : run_amax_rows<false, float>(a, s);
     return rht ? run_amax_rows<true, bf16_t>(a, s) : run_amax_rows<false, bf16_t>(a, s);
+}
+
+template <bool RHT, typename T>
+static cudaError_t run_amax_groups(const QArgs &a, cudaStream_t s) {
+    auto k = k_amax_groups<RHT, T>;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0);
+    const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+    k<<<(int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax_groups(const QArgs &a, bool fp32, bool rht, cudaStream_t s) {
+    if (fp32) return rht ? run_amax_groups<true, float>(a, s) : run_amax_groups<false, float>(a, s);
+    return rht ? run_amax_groups<true, bf16_t>(a, s) : run_amax_groups<false, bf16_t>(a, s);
+}
+
+cudaError_t launch_group_finalize(const QArgs &a, bool rht, bool given, cudaStream_t s) {
+    const int64_t blocks = (a.n_groups + 255) / 256;
+    k_group_finalize<<<(unsigned)blocks, 256, 0, s>>>(a, rht ? 1 : 0, given ? 1 : 0);
+    return cudaGetLastError();
 }
 
 }  // namespace nvfp4

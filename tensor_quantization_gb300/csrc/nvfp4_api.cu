@@ -232,6 +232,59 @@ nvfp4_status nvfp4_quantize_four_over_six(const nvfp4_input *in, uint32_t flags,
     return quantize(in, flags, nvfp4::MODE_4O6_ID, false, 0, 0, 0, out, workspace, stream);
 }
 
+nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const int64_t *group_offsets,
+                                    int64_t n_groups, int32_t mode, uint16_t sign_mask, uint64_t seed,
+                                    uint64_t offset, nvfp4_output *out, void *stream) {
+    nvfp4_status st = check_input(in);
+    if (st != NVFP4_OK) return st;
+    if (!out || (flags & ~(uint32_t)(NVFP4_ROWWISE | NVFP4_SWIZZLED | NVFP4_AMAX_GIVEN | NVFP4_COLWISE |
+                                     NVFP4_BLOCK_2D | NVFP4_SCALE_PER_ROW | NVFP4_FAST_MATH)))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!(flags & NVFP4_ROWWISE)) return NVFP4_ERR_INVALID_ARG;
+    if (flags & (NVFP4_COLWISE | NVFP4_BLOCK_2D | NVFP4_SCALE_PER_ROW | NVFP4_FAST_MATH)) return NVFP4_ERR_UNSUPPORTED;
+    if (mode < NVFP4_MODE_RNE || mode > NVFP4_MODE_FOUR_OVER_SIX) return NVFP4_ERR_INVALID_ARG;
+    if (n_groups < 1 || n_groups > in->rows + 1 || !group_offsets) return NVFP4_ERR_INVALID_ARG;
+    if (in->cols % 16 != 0 || in->col0 != 0) return NVFP4_ERR_INVALID_ARG;
+    if (!out->amax || !out->global_scale) return NVFP4_ERR_INVALID_ARG;
+    const int64_t esz = elem_size(in->dtype);
+    if (in->cols * esz > 96 * 1024) return NVFP4_ERR_UNSUPPORTED;  // rows are staged in shared memory
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool given = flags & NVFP4_AMAX_GIVEN;
+    const bool rht = mode == NVFP4_MODE_RHT_SR;
+    if (in->rows == 0 || in->cols == 0) {
+        if (!given && cudaMemsetAsync(out->amax, 0, n_groups * sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+        return cudaMemsetAsync(out->global_scale, 0, n_groups * sizeof(float), s) == cudaSuccess ? NVFP4_OK
+                                                                                                : NVFP4_ERR_CUDA;
+    }
+    if (!out->codes_row || !out->scales_row || !aligned(out->codes_row, 8)) return NVFP4_ERR_INVALID_ARG;
+
+    nvfp4::QArgs a = make_args(in, out, nullptr, flags);
+    a.sign_mask = sign_mask;
+    a.seed = seed;
+    a.offset = offset;
+    for (int i = 0; i < 10; i++) {
+        a.round_key0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
+        a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+    }
+    a.blk_base = (uint64_t)in->row0 * (uint64_t)(in->cols / 16);
+    a.group_offsets = group_offsets;
+    a.n_groups = n_groups;
+    const bool fp32 = in->dtype == NVFP4_IN_FP32;
+    const int kmode = mode == NVFP4_MODE_RNE ? nvfp4::MODE_RNE_ID
+                      : mode == NVFP4_MODE_FOUR_OVER_SIX ? nvfp4::MODE_4O6_ID
+                                                         : nvfp4::MODE_SR_ID;
+    if (!given) {
+        if (cudaMemsetAsync(out->amax, 0, n_groups * sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+        st = cuda_status(nvfp4::launch_amax_groups(a, fp32, rht, s));
+        if (st != NVFP4_OK) return st;
+    }
+    st = cuda_status(nvfp4::launch_group_finalize(a, rht, given, s));
+    if (st == NVFP4_OK) st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, kmode, rht, s));
+    if (st == NVFP4_OK && (flags & NVFP4_SWIZZLED))
+        st = cuda_status(nvfp4::launch_scale_pad(out->scales_row, in->rows, in->cols / 16, s));
+    return st;
+}
+
 nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *global_scale,
                               int64_t rows, int64_t cols, uint32_t flags, void *out, int32_t out_dtype,
                               void *stream) {

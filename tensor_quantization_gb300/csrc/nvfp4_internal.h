@@ -30,6 +30,10 @@ struct QArgs {
     int swizzled;
     int want_row, want_col;
     int fast_math;  // element quotient as y * RN(1/d)
+    // grouped rowwise scaling: n_groups row ranges [offs[g], offs[g+1]), each
+    // with its own amax / global scale (amax[g] final before the encode)
+    const int64_t *group_offsets;
+    int64_t n_groups;
 };
 
 // Device properties, cached per device.
@@ -55,6 +59,10 @@ cudaError_t launch_quant_col(const QArgs &a, bool fp32, int mode, bool rht, cuda
 cudaError_t launch_quant_2d(const QArgs &a, bool fp32, cudaStream_t s);
 // Rowwise with one global scale per row, amax and quantize in one pass.
 cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
+// Grouped rowwise scaling: per-group amax (atomic maxima into amax[], which the
+// caller has zeroed), then amax[g] / global_scale[g] finalised in place.
+cudaError_t launch_amax_groups(const QArgs &a, bool fp32, bool rht, cudaStream_t s);
+cudaError_t launch_group_finalize(const QArgs &a, bool rht, bool given, cudaStream_t s);
 // Per-tensor rowwise quantize including the amax pass, one cooperative launch
 // (an error return means nothing was enqueued).
 cudaError_t launch_quant_row_fused(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);

@@ -560,6 +560,17 @@ struct RowTables {
     Divisor m6, m4;
 };
 
+// Group of row r: the largest g with group_offsets[g] <= r (binary search).
+__device__ __forceinline__ int64_t group_of(const QArgs &a, int64_t r) {
+    int64_t lo = 0, hi = a.n_groups - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.group_offsets + mid) <= r) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 template <typename T>
 __device__ __forceinline__ void smem_row_block(const uint8_t *rowp, uint32_t j, RawBlock<T> &b) {
     const uint4 *p = reinterpret_cast<const uint4 *>(rowp + (size_t)j * 16 * sizeof(T));
@@ -601,6 +612,7 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
     __shared__ RowTables tabs[2];
     __shared__ RhtMult rm;
     __shared__ uint32_t red[2][8];
+    __shared__ float group_amax[2];
     __shared__ __align__(8) uint64_t full[kRowBufs];
     uint8_t *bufs = dyn_smem + ((16u - (smem_addr(dyn_smem) & 15u)) & 15u);
     const uint32_t CS = (uint32_t)(a.cols >> 4);
@@ -630,9 +642,13 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
         const bool arrived = mbar_wait(&full[s], (k / kRowBufs) & 1u);
         if (!arrived) atomicAdd(&g_wait_timeouts, 1u);
         const uint8_t *rowp = bufs + s * buf_bytes;
-        // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max)
-        uint32_t mb;
-        if (RHT) {
+        // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max);
+        // grouped scaling instead reads the final amax of the row's group
+        const bool grouped = a.n_groups > 0;
+        if (grouped && tid == 0) group_amax[par] = a.amax[group_of(a, r)];
+        uint32_t mb = 0;
+        if (grouped) {
+        } else if (RHT) {
             float m = 0.0f;
             for (uint32_t j = tid; j < CS; j += nt) {
                 RawBlock<T> raw;
@@ -663,6 +679,7 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
         }
         float A = __uint_as_float(mb);
         if (RHT) A = __fmul_rn(A, 0.25f);
+        if (grouped) A = group_amax[par];
         const float g = global_scale_of(A);
         RowTables &tb = tabs[par];
         for (int e = tid; e < 130; e += nt) {
@@ -673,7 +690,9 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
         }
         // a row whose copy never arrived is published with a NaN scale
         const bool lost = __syncthreads_or(!arrived);  // (2) tables ready
-        if (tid == 0) {
+        if (tid == 0 && grouped) {
+            if (lost) a.gscale[group_of(a, r)] = __uint_as_float(0x7FFFFFFFu);
+        } else if (tid == 0) {
             a.amax[r] = A;
             a.gscale[r] = lost ? __uint_as_float(0x7FFFFFFFu) : g;
         }

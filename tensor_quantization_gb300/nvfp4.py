@@ -45,7 +45,8 @@ class Output(ctypes.Structure):
 
 EXPORTS = ("nvfp4_workspace_bytes", "nvfp4_scale_bytes", "nvfp4_amax", "nvfp4_quantize_rne",
            "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr", "nvfp4_quantize_four_over_six",
-           "nvfp4_dequantize", "nvfp4_status_string", "nvfp4_quantize_rht_sr_static")
+           "nvfp4_dequantize", "nvfp4_status_string", "nvfp4_quantize_rht_sr_static", "nvfp4_quantize_grouped")
+MODE_RNE, MODE_SR, MODE_RHT_SR, MODE_FOUR_OVER_SIX = 0, 1, 2, 3
 
 
 def lib_path() -> str:
@@ -75,8 +76,10 @@ def load(path: str | None = None):
     L.nvfp4_quantize_four_over_six.argtypes = [PI, u32, PO, vp, vp]
     L.nvfp4_quantize_rht_sr_static.argtypes = [PI, u32, ctypes.c_uint16, u64, u64, PO, vp]
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, u32, vp, i32, vp]
+    L.nvfp4_quantize_grouped.argtypes = [PI, u32, vp, i64, i32, ctypes.c_uint16, u64, u64, PO, vp]
     for f in ("nvfp4_amax", "nvfp4_quantize_rne", "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr",
-              "nvfp4_quantize_four_over_six", "nvfp4_dequantize", "nvfp4_quantize_rht_sr_static"):
+              "nvfp4_quantize_four_over_six", "nvfp4_dequantize", "nvfp4_quantize_rht_sr_static",
+              "nvfp4_quantize_grouped"):
         getattr(L, f).restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -176,6 +179,14 @@ def nvfp4_quantize_four_over_six(x, flags, out: Output, workspace, stream=None) 
                                                _ptr(workspace), _stream(stream)), "nvfp4_quantize_four_over_six")
 
 
+def nvfp4_quantize_grouped(x, flags, group_offsets, n_groups, mode, sign_mask, seed, offset, out: Output,
+                           stream=None) -> None:
+    """Grouped rowwise quantize; group_offsets: int64 CUDA tensor of n_groups+1 row offsets."""
+    _check(load().nvfp4_quantize_grouped(ctypes.byref(_input(x)), flags, _ptr(group_offsets), n_groups, mode,
+                                         sign_mask & 0xFFFF, seed, offset, ctypes.byref(out), _stream(stream)),
+           "nvfp4_quantize_grouped")
+
+
 def nvfp4_dequantize(codes, scales, global_scale, rows, cols, flags, out, stream=None) -> None:
     if out.dtype == torch.bfloat16:
         dt = IN_BF16
@@ -258,6 +269,27 @@ def quantize(x: torch.Tensor, *, mode: str = "rne", rowwise: bool = True, colwis
             nvfp4_quantize_four_over_six(xin, flags, o, ws, stream)
         else:
             raise ValueError(f"unknown mode {mode}")
+    return q
+
+
+def quantize_grouped(x: torch.Tensor, group_offsets: torch.Tensor, *, mode: str = "rne", swizzled: bool = False,
+                     sign_mask: int = 0, seed: int = 0, offset: int = 0, amax: torch.Tensor | None = None,
+                     stream=None) -> Quantized:
+    """Rowwise quantize of the row groups [offs[g], offs[g+1]) of x, each with its
+    own amax and global scale (n_groups of each)."""
+    n = group_offsets.numel() - 1
+    flags = ROWWISE | (SWIZZLED if swizzled else 0) | (AMAX_GIVEN if amax is not None else 0)
+    R, C = x.shape
+    q = Quantized(torch.empty(R, C // 2, dtype=torch.uint8, device=x.device),
+                  torch.empty(nvfp4_scale_bytes(R, C, flags), dtype=torch.uint8, device=x.device), None, None,
+                  torch.empty(n, dtype=torch.float32, device=x.device),
+                  torch.empty(n, dtype=torch.float32, device=x.device), flags)
+    if amax is not None:
+        q.amax.copy_(amax)
+    m = {"rne": MODE_RNE, "sr": MODE_SR, "rht_sr": MODE_RHT_SR, "4o6": MODE_FOUR_OVER_SIX}[mode]
+    o = make_output(q.codes_row, q.scales_row, None, None, q.amax, q.global_scale)
+    with torch.cuda.device(x.device):
+        nvfp4_quantize_grouped(x, flags, group_offsets, n, m, sign_mask, seed, offset, o, stream)
     return q
 
 

@@ -85,6 +85,18 @@ def test_arguments_are_rejected_before_any_launch(lib):
         nvfp4.ERR_UNSUPPORTED
     assert sr(ctypes.byref(_inp(16, 32, 32, row0=16)), 2, 1, 0, ctypes.byref(out), ws, None) == \
         nvfp4.ERR_UNSUPPORTED
+    grp = lib.nvfp4_quantize_grouped
+    offs = ctypes.c_void_p(64)
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 1, offs, 0, 0, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_INVALID_ARG  # no groups
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 1, offs, 2, 9, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_INVALID_ARG  # mode
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 3, offs, 2, 0, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_UNSUPPORTED  # columnwise
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 1 | nvfp4.FAST_MATH, offs, 2, 0, 0, 0, 0, ctypes.byref(out),
+               None) == nvfp4.ERR_UNSUPPORTED
+    assert grp(ctypes.byref(_inp(2, 65536, 65536)), 1, offs, 2, 0, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_UNSUPPORTED  # a 128 KiB row does not fit the row buffer
     dq = lib.nvfp4_dequantize
     assert dq(16, 16, 16, 4, 24, 0, 16, 0, None) == nvfp4.ERR_INVALID_ARG  # cols % 16
     assert dq(16, 16, 16, 4, 32, 0, 16, 9, None) == nvfp4.ERR_INVALID_ARG  # dtype

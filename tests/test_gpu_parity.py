@@ -559,3 +559,83 @@ def test_two_kernel_rowwise_path_ragged(mode, dtype):
     kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", swizzled=True, sign_mask=0x2222,
               seed=12, offset=1)
     assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+
+
+# ------------------------------------------------------ grouped scaling
+def _oracle_grouped(x, offs, *, mode, swizzled, sign_mask=0, seed=0, offset=0, amax=None):
+    """Each row group quantized as a tensor of its own, Philox blocks numbered in
+    the whole input (the oracle's row range of the full tensor with the group's
+    amax given)."""
+    xn = np_bits(x)
+    R, C = x.shape
+    CS = C // 16
+    codes = np.zeros((R, C // 2), np.uint8)
+    lin = np.zeros((R, CS), np.uint8)
+    amaxes, gscales = [], []
+    kw = dict(mode="sr" if mode == "rht_sr" else mode, rht=mode == "rht_sr", sign_mask=sign_mask, seed=seed,
+              offset=offset)
+    for g in range(len(offs) - 1):
+        o0, o1 = int(offs[g]), int(offs[g + 1])
+        if o1 == o0:
+            A = 0.0 if amax is None else float(amax[g])
+            amaxes.append(np.float32(A))
+            gscales.append(np.float32(np.float32(A) / np.float32(2688.0)))
+            continue
+        if amax is None:
+            A, _ = oracle.amax(xn[o0:o1], rht=kw["rht"], sign_mask=sign_mask)
+            A = float(np.asarray(A).ravel()[0])
+        else:
+            A = float(amax[g])
+        o = oracle.quantize(xn, row_range=(o0, o1), amax_given=A, **kw)
+        codes[o0:o1] = o["codes"][o0:o1]
+        lin[o0:o1] = o["scales"].reshape(R, CS)[o0:o1]
+        amaxes.append(np.asarray(o["amax"]).ravel()[0])
+        gscales.append(np.asarray(o["global_scale"]).ravel()[0])
+    if swizzled:
+        csp = (CS + 3) // 4 * 4
+        out = np.zeros(oracle.scale_bytes(R, C, True), np.uint8)
+        for r in range(R):
+            for j in range(CS):
+                out[oracle.swizzle_offset(r, j, csp)] = lin[r, j]
+        scales = out
+    else:
+        scales = lin.ravel()
+    return codes, scales, np.array(amaxes, np.float32), np.array(gscales, np.float32)
+
+
+@pytest.mark.parametrize("mode", ["rne", "sr", "rht_sr", "4o6"])
+@pytest.mark.parametrize("swizzled", [False, True], ids=["linear", "swizzled"])
+def test_grouped_rows_each_with_its_own_scale(mode, swizzled):
+    """Row groups of very different magnitudes (an empty group and a one-row
+    group included) against the oracle run per group."""
+    x = mixed_input(300, 256, seed=27)
+    offs = [0, 40, 40, 41, 170, 300]
+    x[41:170] *= 1e-3  # a group of much smaller values: its own scale matters
+    kw = dict(mode=mode, swizzled=swizzled, sign_mask=0x6A6A, seed=14, offset=3)
+    offs_d = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    q = nvfp4.quantize_grouped(to_device(x), offs_d, **kw)
+    torch.cuda.synchronize()
+    codes, scales, amaxes, gscales = _oracle_grouped(x, offs, **kw)
+    assert np.array_equal(q.codes_row.cpu().numpy(), codes)
+    assert np.array_equal(q.scales_row.cpu().numpy(), scales)
+    assert same_float_bits(q.amax.cpu().numpy(), amaxes)
+    assert same_float_bits(q.global_scale.cpu().numpy(), gscales)
+    # the same with the amaxes given
+    A = torch.from_numpy(amaxes * np.float32(2.0)).cuda()
+    q2 = nvfp4.quantize_grouped(to_device(x), offs_d, amax=A, **kw)
+    torch.cuda.synchronize()
+    codes2, scales2, _, gscales2 = _oracle_grouped(x, offs, amax=amaxes * np.float32(2.0), **kw)
+    assert np.array_equal(q2.codes_row.cpu().numpy(), codes2)
+    assert np.array_equal(q2.scales_row.cpu().numpy(), scales2)
+    assert same_float_bits(q2.global_scale.cpu().numpy(), gscales2)
+
+
+def test_grouped_one_group_is_the_per_tensor_result():
+    x = mixed_input(256, 512, seed=28)
+    offs_d = torch.tensor([0, 256], dtype=torch.int64, device="cuda")
+    q = nvfp4.quantize_grouped(to_device(x), offs_d, mode="sr", seed=3, swizzled=True)
+    torch.cuda.synchronize()
+    o = oracle_run(x, mode="sr", seed=3, swizzled=True)
+    assert np.array_equal(q.codes_row.cpu().numpy(), o["codes_row"])
+    assert np.array_equal(q.scales_row.cpu().numpy(), o["scales_row"])
+    assert same_float_bits(q.amax.cpu().numpy(), o["amax"])
