@@ -76,6 +76,10 @@ def _lib():
         lib.ora_e2m1_sr_n.restype = None
         lib.ora_e4m3_rn_n.argtypes = [vp, i64, vp]
         lib.ora_e4m3_rn_n.restype = None
+        lib.ora_inverse_rht16.argtypes = [vp, u32]
+        lib.ora_inverse_rht16.restype = None
+        lib.ora_dequantize_rht.argtypes = [vp, vp, vp, i64, i64, i32, i32, u32, vp, i32]
+        lib.ora_dequantize_rht.restype = i32
         lib.ora_candidate_error_n.argtypes = [vp, vp, vp, vp, i64, vp]
         lib.ora_candidate_error_n.restype = None
         lib.ora_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -240,4 +244,26 @@ def candidate_error_array(y: np.ndarray, codes: np.ndarray, S: np.ndarray, g: np
     g = np.ascontiguousarray(g, np.float32).ravel()
     out = np.zeros(len(y), np.float32)
     _lib().ora_candidate_error_n(_ptr(y), _ptr(codes), _ptr(S), _ptr(g), len(y), _ptr(out))
+    return out
+
+
+def inverse_rht16(y, sign_mask: int) -> np.ndarray:
+    """Inverse of rht16: signs on the inputs, the butterfly, then x 0.25."""
+    y = np.ascontiguousarray(y, np.float32).copy()
+    _lib().ora_inverse_rht16(_ptr(y), sign_mask & 0xFFFF)
+    return y
+
+
+def dequantize_rht(codes: np.ndarray, scales: np.ndarray, global_scale: np.ndarray, rows: int, cols: int, *,
+                   sign_mask: int, swizzled: bool = False, per_row: bool = False,
+                   out_dtype: str = "fp32") -> np.ndarray:
+    """Standard decode followed by the inverse RHT of every 16-block."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    gs = np.ascontiguousarray(global_scale, np.float32)
+    out = np.zeros((rows, cols), np.uint16 if out_dtype == "bf16" else np.float32)
+    rc = _lib().ora_dequantize_rht(_ptr(codes), _ptr(scales), _ptr(gs), rows, cols, int(swizzled), int(per_row),
+                                   sign_mask & 0xFFFF, _ptr(out), 0 if out_dtype == "bf16" else 1)
+    if rc != 0:
+        raise ValueError(f"ora_dequantize_rht failed ({rc})")
     return out

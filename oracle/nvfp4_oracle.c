@@ -427,6 +427,52 @@ int ora_dequantize(const uint8_t *codes, const uint8_t *scales, const float *gsc
     return ORA_OK;
 }
 
+/* Inverse of the 16-point RHT: y = (v.H16).(1/4).diag(s) gives
+ * v = ((y.diag(s)).H16).(1/4), because H16.H16 = 16 I.  Steps: the signs on
+ * the inputs, the same butterfly (strides 1, 2, 4, 8), then x 0.25. */
+void ora_inverse_rht16(float y[16], uint32_t sign_mask) {
+    for (int j = 0; j < 16; j++)
+        if ((sign_mask >> j) & 1u) y[j] = -y[j];
+    for (int h = 1; h < 16; h <<= 1)
+        for (int i = 0; i < 16; i++)
+            if ((i & h) == 0) {
+                float a = y[i], b = y[i + h];
+                y[i] = a + b;
+                y[i + h] = a - b;
+            }
+    for (int j = 0; j < 16; j++) y[j] = y[j] * 0.25f;
+}
+
+/* Dequantize of an RHT-quantized rowwise output back to the original basis:
+ * the standard decode of each 16-block (as ora_dequantize, fp32), then the
+ * inverse RHT of the block; a bf16 output takes RN of the result. */
+int ora_dequantize_rht(const uint8_t *codes, const uint8_t *scales, const float *gscale,
+                       int64_t rows, int64_t cols, int swizzled, int per_row, uint32_t sign_mask,
+                       void *out, int out_dtype) {
+    if (!codes || !scales || !gscale || !out || cols % 16 != 0 || rows < 0) return ORA_ERR_ARG;
+    int64_t CS = cols / 16;
+    float y[16];
+    for (int64_t r = 0; r < rows; r++) {
+        float g = per_row ? gscale[r] : gscale[0];
+        for (int64_t j = 0; j < CS; j++) {
+            float Sf = ora_e4m3_value(get_scale(scales, r, j, CS, swizzled));
+            float d = Sf * g;
+            for (int e = 0; e < 16; e++) {
+                unsigned byte = codes[r * (cols / 2) + 8 * j + e / 2];
+                int code = (e & 1) ? (int)(byte >> 4) : (int)(byte & 15u);
+                y[e] = ora_e2m1_value(code) * d;
+            }
+            ora_inverse_rht16(y, sign_mask);
+            for (int e = 0; e < 16; e++) {
+                int64_t c = 16 * j + e;
+                if (out_dtype == 0) ((uint16_t *)out)[r * cols + c] = ora_f32_to_bf16(y[e]);
+                else ((float *)out)[r * cols + c] = y[e];
+            }
+        }
+    }
+    return ORA_OK;
+}
+
 /* Global amax alone (per tensor, or per output row), same definition as in
  * ora_quantize. */
 int ora_amax(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld, int orient,

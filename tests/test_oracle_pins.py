@@ -518,3 +518,43 @@ def test_dequantize_definition_on_exact_cases():
     expect = [vals[1], vals[2], vals[3], vals[4], vals[5], vals[6], vals[7], -0.0, -vals[1], -vals[2],
               -vals[3], -vals[4], -vals[5], -vals[6], -vals[7], 0.0]
     assert out[0].tolist() == [2.0 * v for v in expect]
+
+
+# -------------------------------------------------- inverse RHT (decode side)
+def test_inverse_rht_is_exact_on_small_integers():
+    """v = ((y o s) H16) / 4: exact in rationals for small integers, and the
+    inverse undoes the forward transform bit for bit there."""
+    rng = np.random.default_rng(40)
+    H = np.array(hadamard16(), dtype=object)
+    for _ in range(200):
+        mask = int(rng.integers(0, 1 << 16))
+        y = rng.integers(-64, 65, 16).astype(np.float32) * np.float32(0.25)
+        s = np.array([-1 if (mask >> j) & 1 else 1 for j in range(16)], dtype=object)
+        want = [Fraction(sum(Fraction(float(y[k])) * s[k] * H[k][j] for k in range(16)), 4) for j in range(16)]
+        got = oracle.inverse_rht16(y, mask)
+        assert [Fraction(float(g)) for g in got] == want
+        v = rng.integers(-100, 101, 16).astype(np.float32)
+        assert np.array_equal(oracle.inverse_rht16(oracle.rht16(v, mask), mask), v)
+
+
+def test_rht_dequantize_preserves_the_block_error_norm():
+    """H16/4 is orthogonal, so mapping a dequantized block back through the
+    inverse RHT keeps its distance to the source: ||x - x^||2 = ||y - y^||2 per
+    block (up to fp32 rounding).  A wrong sign placement or transposed inverse
+    breaks the equality."""
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((32, 256)) * np.exp(rng.standard_normal((32, 1)))).astype(np.float32)
+    mask = 0x5AC3
+    o = oracle.quantize(x, mode="sr", rht=True, sign_mask=mask, seed=4)
+    xr = oracle.dequantize_rht(o["codes"], o["scales"], o["global_scale"], 32, 256, sign_mask=mask)
+    yd = oracle.dequantize(o["codes"], o["scales"], o["global_scale"], 32, 256)
+    y = np.stack([oracle.rht16(b, mask) for b in x.reshape(-1, 16)]).reshape(32, 256)
+    ex = np.linalg.norm((x.astype(np.float64) - xr).reshape(-1, 16), axis=1)
+    ey = np.linalg.norm((y.astype(np.float64) - yd).reshape(-1, 16), axis=1)
+    scale = np.linalg.norm(x.astype(np.float64).reshape(-1, 16), axis=1)
+    assert np.all(np.abs(ex - ey) <= 1e-5 * scale + 1e-30)
+    assert np.all(ex <= 0.5 * scale)  # and the decode is close to the source at all
+    # the inverse of a wrong mask does not give the same error
+    bad = oracle.dequantize_rht(o["codes"], o["scales"], o["global_scale"], 32, 256, sign_mask=mask ^ 1)
+    eb = np.linalg.norm((x.astype(np.float64) - bad).reshape(-1, 16), axis=1)
+    assert np.mean(np.abs(eb - ey) > 1e-3 * scale) > 0.5
