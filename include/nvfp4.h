@@ -234,6 +234,18 @@ nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const
                               int64_t rows, int64_t cols, uint32_t flags, void *out, int32_t out_dtype,
                               void *stream);
 
+/* Decode of codes produced with the RHT (nvfp4_quantize_rht_sr, rowwise or
+ * columnwise output), mapped back to the source basis: the standard decode of
+ * each 16-block as nvfp4_dequantize (fp32), then the inverse transform
+ * v = ((y . diag(s)) . H16) / 4 (signs on the inputs, the butterfly with
+ * strides 1, 2, 4, 8, then x 0.25), then the output rounding.  sign_mask is the
+ * one the codes were produced with.  For a columnwise output pass
+ * rows = cols of X and cols = rows of X: the result is then X^T.  Arguments
+ * and checks as nvfp4_dequantize. */
+nvfp4_status nvfp4_dequantize_rht(const uint8_t *codes, const uint8_t *scales, const float *global_scale,
+                                  int64_t rows, int64_t cols, uint32_t flags, uint16_t sign_mask, void *out,
+                                  int32_t out_dtype, void *stream);
+
 /* Human-readable name of a status. */
 const char *nvfp4_status_string(nvfp4_status status);
 

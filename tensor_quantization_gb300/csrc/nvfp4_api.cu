@@ -285,9 +285,9 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
     return st;
 }
 
-nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *global_scale,
-                              int64_t rows, int64_t cols, uint32_t flags, void *out, int32_t out_dtype,
-                              void *stream) {
+static nvfp4_status dequantize(const uint8_t *codes, const uint8_t *scales, const float *global_scale, int64_t rows,
+                               int64_t cols, uint32_t flags, int rht, uint32_t sign_mask, void *out, int32_t out_dtype,
+                               void *stream) {
     if (flags & ~(uint32_t)(NVFP4_SWIZZLED | NVFP4_SCALE_PER_ROW)) return NVFP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0 || rows >= kMaxDim || cols >= kMaxDim || rows * cols > kMaxElems || cols % 16 != 0)
         return NVFP4_ERR_INVALID_ARG;
@@ -297,7 +297,20 @@ nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const
         return NVFP4_ERR_INVALID_ARG;
     return cuda_status(nvfp4::launch_dequant(codes, scales, global_scale, rows, cols,
                                              (flags & NVFP4_SWIZZLED) ? 1 : 0, (flags & NVFP4_SCALE_PER_ROW) ? 1 : 0,
-                                             out, out_dtype == NVFP4_IN_FP32, static_cast<cudaStream_t>(stream)));
+                                             out, out_dtype == NVFP4_IN_FP32, rht, sign_mask,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *global_scale,
+                              int64_t rows, int64_t cols, uint32_t flags, void *out, int32_t out_dtype,
+                              void *stream) {
+    return dequantize(codes, scales, global_scale, rows, cols, flags, 0, 0, out, out_dtype, stream);
+}
+
+nvfp4_status nvfp4_dequantize_rht(const uint8_t *codes, const uint8_t *scales, const float *global_scale,
+                                  int64_t rows, int64_t cols, uint32_t flags, uint16_t sign_mask, void *out,
+                                  int32_t out_dtype, void *stream) {
+    return dequantize(codes, scales, global_scale, rows, cols, flags, 1, sign_mask, out, out_dtype, stream);
 }
 
 const char *nvfp4_status_string(nvfp4_status status) {

@@ -3,7 +3,10 @@
 // Decode ("[nvfp4 training][rl] Add a CuTe DSL fast-path kernel for
 // four-over-six quantize #4852", PR description: nvfp4_dequantize, the
 // standard NVFP4 decode): out = value(code) * (Sf * g), each product rounded
-// to fp32, then to bf16 (round to nearest even) for a bf16 output.
+// to fp32, then to bf16 (round to nearest even) for a bf16 output.  With the
+// inverse RHT (codes of an RHT-quantized output), each decoded 16-block is
+// mapped back to the source basis before the output rounding: signs on the
+// inputs, the butterfly with strides 1, 2, 4, 8, then x 0.25.
 #include <cuda_bf16.h>
 
 #include "nvfp4_encode.cuh"
@@ -13,7 +16,12 @@ namespace nvfp4 {
 
 __global__ void __launch_bounds__(256) k_dequant(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales,
                                                  const float *__restrict__ gscale, int64_t rows, int64_t cols,
-                                                 int swizzled, int per_row, void *out, int out_fp32) {
+                                                 int swizzled, int per_row, void *out, int out_fp32, int rht,
+                                                 uint32_t sign_mask) {
+    f2 sgn[8];  // +-1 per input element of the inverse RHT
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+        sgn[k] = f2{((sign_mask >> (2 * k)) & 1u) ? -1.0f : 1.0f, ((sign_mask >> (2 * k + 1)) & 1u) ? -1.0f : 1.0f};
     const uint32_t CS = (uint32_t)(cols >> 4);
     const uint32_t n = (uint32_t)rows * CS;
     const int64_t csp = (CS + 3) & ~3u;
@@ -28,6 +36,13 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t *__restrict__ cod
         for (int k = 0; k < 8; k++) {
             const uint32_t w = (k < 4) ? c.x : c.y;
             o[k] = mul2(e2m1x2_value(w >> (8 * (k & 3))), f2{d, d});
+        }
+        if (rht) {
+#pragma unroll
+            for (int k = 0; k < 8; k++) o[k] = mul2(o[k], sgn[k]);
+            fwht16(o);
+#pragma unroll
+            for (int k = 0; k < 8; k++) o[k] = mul2(o[k], f2{0.25f, 0.25f});
         }
         const int64_t base = (int64_t)r * cols + 16 * j;
         if (out_fp32) {
@@ -77,13 +92,15 @@ cudaError_t launch_scale_pad(uint8_t *scales, int64_t rows_out, int64_t cs, cuda
 }
 
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *gscale, int64_t rows,
-                           int64_t cols, int swizzled, int per_row, void *out, int out_fp32, cudaStream_t s) {
+                           int64_t cols, int swizzled, int per_row, void *out, int out_fp32, int rht,
+                           uint32_t sign_mask, cudaStream_t s) {
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dequant, 256, 0);
     const int64_t want = (rows * (cols >> 4) + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
     const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-    k_dequant<<<grid, 256, 0, s>>>(codes, scales, gscale, rows, cols, swizzled, per_row, out, out_fp32);
+    k_dequant<<<grid, 256, 0, s>>>(codes, scales, gscale, rows, cols, swizzled, per_row, out, out_fp32, rht,
+                                   sign_mask);
     return cudaGetLastError();
 }
 

@@ -77,6 +77,7 @@ cudaError_t launch_quant_row_fused_approx(const QArgs &a, bool fp32, int mode, b
 cudaError_t launch_scale_pad(uint8_t *scales, int64_t rows_out, int64_t cs, cudaStream_t s);
 
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *gscale, int64_t rows,
-                           int64_t cols, int swizzled, int per_row, void *out, int out_fp32, cudaStream_t s);
+                           int64_t cols, int swizzled, int per_row, void *out, int out_fp32, int rht,
+                           uint32_t sign_mask, cudaStream_t s);
 
 }  // namespace nvfp4

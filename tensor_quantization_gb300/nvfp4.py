@@ -45,7 +45,8 @@ class Output(ctypes.Structure):
 
 EXPORTS = ("nvfp4_workspace_bytes", "nvfp4_scale_bytes", "nvfp4_amax", "nvfp4_quantize_rne",
            "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr", "nvfp4_quantize_four_over_six",
-           "nvfp4_dequantize", "nvfp4_status_string", "nvfp4_quantize_rht_sr_static", "nvfp4_quantize_grouped")
+           "nvfp4_dequantize", "nvfp4_status_string", "nvfp4_quantize_rht_sr_static", "nvfp4_quantize_grouped",
+           "nvfp4_dequantize_rht")
 MODE_RNE, MODE_SR, MODE_RHT_SR, MODE_FOUR_OVER_SIX = 0, 1, 2, 3
 
 
@@ -77,9 +78,10 @@ def load(path: str | None = None):
     L.nvfp4_quantize_rht_sr_static.argtypes = [PI, u32, ctypes.c_uint16, u64, u64, PO, vp]
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, u32, vp, i32, vp]
     L.nvfp4_quantize_grouped.argtypes = [PI, u32, vp, i64, i32, ctypes.c_uint16, u64, u64, PO, vp]
+    L.nvfp4_dequantize_rht.argtypes = [vp, vp, vp, i64, i64, u32, ctypes.c_uint16, vp, i32, vp]
     for f in ("nvfp4_amax", "nvfp4_quantize_rne", "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr",
               "nvfp4_quantize_four_over_six", "nvfp4_dequantize", "nvfp4_quantize_rht_sr_static",
-              "nvfp4_quantize_grouped"):
+              "nvfp4_quantize_grouped", "nvfp4_dequantize_rht"):
         getattr(L, f).restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -187,15 +189,23 @@ def nvfp4_quantize_grouped(x, flags, group_offsets, n_groups, mode, sign_mask, s
            "nvfp4_quantize_grouped")
 
 
-def nvfp4_dequantize(codes, scales, global_scale, rows, cols, flags, out, stream=None) -> None:
+def _out_dtype(out) -> int:
     if out.dtype == torch.bfloat16:
-        dt = IN_BF16
-    elif out.dtype == torch.float32:
-        dt = IN_FP32
-    else:
-        raise ValueError("output must be bfloat16 or float32")
+        return IN_BF16
+    if out.dtype == torch.float32:
+        return IN_FP32
+    raise ValueError("output must be bfloat16 or float32")
+
+
+def nvfp4_dequantize(codes, scales, global_scale, rows, cols, flags, out, stream=None) -> None:
     _check(load().nvfp4_dequantize(_ptr(codes), _ptr(scales), _ptr(global_scale), rows, cols, flags, _ptr(out),
-                                   dt, _stream(stream)), "nvfp4_dequantize")
+                                   _out_dtype(out), _stream(stream)), "nvfp4_dequantize")
+
+
+def nvfp4_dequantize_rht(codes, scales, global_scale, rows, cols, flags, sign_mask, out, stream=None) -> None:
+    _check(load().nvfp4_dequantize_rht(_ptr(codes), _ptr(scales), _ptr(global_scale), rows, cols, flags,
+                                       sign_mask & 0xFFFF, _ptr(out), _out_dtype(out), _stream(stream)),
+           "nvfp4_dequantize_rht")
 
 
 # ------------------------------------------------------------ conveniences
@@ -294,9 +304,14 @@ def quantize_grouped(x: torch.Tensor, group_offsets: torch.Tensor, *, mode: str 
 
 
 def dequantize(codes: torch.Tensor, scales: torch.Tensor, global_scale: torch.Tensor, rows: int, cols: int, *,
-               swizzled: bool = False, per_row: bool = False, out_dtype=torch.float32, stream=None) -> torch.Tensor:
+               swizzled: bool = False, per_row: bool = False, out_dtype=torch.float32,
+               rht_sign_mask: int | None = None, stream=None) -> torch.Tensor:
+    """Standard decode; with rht_sign_mask, also the inverse RHT of every block."""
     out = torch.empty(rows, cols, dtype=out_dtype, device=codes.device)
     flags = (SWIZZLED if swizzled else 0) | (SCALE_PER_ROW if per_row else 0)
     with torch.cuda.device(codes.device):
-        nvfp4_dequantize(codes, scales, global_scale, rows, cols, flags, out, stream)
+        if rht_sign_mask is None:
+            nvfp4_dequantize(codes, scales, global_scale, rows, cols, flags, out, stream)
+        else:
+            nvfp4_dequantize_rht(codes, scales, global_scale, rows, cols, flags, rht_sign_mask, out, stream)
     return out

@@ -639,3 +639,36 @@ def test_grouped_one_group_is_the_per_tensor_result():
     assert np.array_equal(q.codes_row.cpu().numpy(), o["codes_row"])
     assert np.array_equal(q.scales_row.cpu().numpy(), o["scales_row"])
     assert same_float_bits(q.amax.cpu().numpy(), o["amax"])
+
+
+@pytest.mark.parametrize("swizzled", [False, True])
+@pytest.mark.parametrize("per_row", [False, True])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_dequantize_with_inverse_rht(swizzled, per_row, out_dtype):
+    x = mixed_input(136, 224, seed=29)
+    mask = 0xC3A5
+    o = oracle.quantize(np_bits(x), mode="sr", rht=True, sign_mask=mask, per_row=per_row, swizzled=swizzled,
+                        seed=7)
+    dt = "bf16" if out_dtype == torch.bfloat16 else "fp32"
+    ref = oracle.dequantize_rht(o["codes"], o["scales"], o["global_scale"], 136, 224, sign_mask=mask,
+                                swizzled=swizzled, per_row=per_row, out_dtype=dt)
+    got = nvfp4.dequantize(torch.from_numpy(o["codes"]).cuda(), torch.from_numpy(o["scales"].ravel()).cuda(),
+                           torch.from_numpy(o["global_scale"]).cuda(), 136, 224, swizzled=swizzled,
+                           per_row=per_row, out_dtype=out_dtype, rht_sign_mask=mask)
+    torch.cuda.synchronize()
+    if out_dtype == torch.bfloat16:
+        assert np.array_equal(got.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+    else:
+        assert same_float_bits(got.cpu().numpy(), ref)
+
+
+def test_rht_round_trip_through_the_library():
+    """quantize(RHT+SR) then dequantize with the inverse RHT lands near the source."""
+    x = mixed_input(256, 512, seed=30, dtype=torch.float32)
+    xd = x.cuda()
+    q = nvfp4.quantize(xd, mode="sr", rht=True, sign_mask=0x0F0F, seed=8, swizzled=True)
+    back = nvfp4.dequantize(q.codes_row, q.scales_row, q.global_scale, 256, 512, swizzled=True,
+                            rht_sign_mask=0x0F0F)
+    torch.cuda.synchronize()
+    err = (back.cpu() - x).reshape(-1, 16).norm(dim=1)
+    assert float((err <= 0.5 * x.reshape(-1, 16).norm(dim=1) + 1e-30).float().mean()) > 0.99
