@@ -387,10 +387,7 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
                       else "k_quant_rowscaled")
     if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
         return None, "k_quant_row_fused"
-    if not w.rht:
-        amax = "k_amax_plain"
-    else:
-        amax = "k_amax_rht_col" if (w.colwise and not w.rowwise) else "k_amax_rht_row"
+    amax = "k_amax_rht_col" if (w.rht and w.colwise and not w.rowwise) else "k_amax_tma"
     if w.block2d:
         return amax, "k_quant_2d"
     if w.colwise and not w.rowwise:

@@ -1,8 +1,9 @@
 // nvfp4_amax.cu -- global amax reductions.
 //
-// Per tensor: grid-stride 128-bit loads, magnitude-bit maximum per thread,
-// warp (redux.sync) and CTA trees, then ONE atomicMax per CTA into the
-// workspace.  The CTA that takes the last ticket publishes amax and
+// Per tensor: rowwise blocks (and the plain maximum of any orientation) are
+// streamed through shared memory by TMA; columnwise RHT blocks are read as
+// 16-row strips.  Magnitude-bit maximum per thread, warp (redux.sync) and CTA
+// trees, then ONE atomicMax per CTA into the workspace.  The CTA that takes the last ticket publishes amax and
 // g = amax / 2688 and returns the workspace to zero, so the pass needs no
 // memset and no second launch.  The host never waits: the per-tensor scale
 // stays on the device ("nvfp4-sm120" README, section "Results": the amax host
@@ -14,6 +15,7 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tiles.cuh"
 #include "nvfp4_tma.cuh"
 
 namespace nvfp4 {
@@ -38,74 +40,90 @@ __device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, 
     }
 }
 
-// No RHT: the maximum over every element, any orientation.  A thread takes
-// kPlainUnroll 16-byte chunks per step (all loads issued before any is
-// used), so enough bytes are in flight to stream at HBM rate.
-constexpr int kPlainUnroll = 4;
-
-template <typename T>
-__global__ void __launch_bounds__(256) k_amax_plain(const QArgs a) {
-    constexpr int W = Chunk<T>::W;
-    const uint32_t NCH = (uint32_t)((a.cols + W - 1) / W);
-    const uint32_t n = (uint32_t)a.rows * NCH;
-    const T *x = static_cast<const T *>(a.x);
-    const uint32_t stride = gridDim.x * blockDim.x;
-    uint32_t m = 0;
-    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += kPlainUnroll * stride) {
-        Chunk<T> c[kPlainUnroll];
+// Unsigned maximum of the magnitude bits of a raw block (bf16: two 16-bit
+// lanes per word, compared as integers; NaN patterns sort above +inf).
+__device__ __forceinline__ uint32_t block_max_bits(const RawBlock<bf16_t> &b) {
+    uint32_t t[2];
 #pragma unroll
-        for (int u = 0; u < kPlainUnroll; u++) {
-            const uint32_t i = i0 + u * stride;
-            if (i < n) {
-                const uint32_t r = i / NCH, ch = i - r * NCH;
-                const int64_t c0 = (int64_t)ch * W;
-                c[u].load(x + (int64_t)r * a.ld + c0, (int)min((int64_t)W, a.cols - c0));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPlainUnroll; u++)
-            if (i0 + u * stride < n)
-#pragma unroll
-                for (int e = 0; e < W; e++) m = max(m, mag_bits(c[u].get(e)));
+    for (int k = 0; k < 2; k++) {
+        uint32_t u, v;
+        asm("max.u16x2 %0, %1, %2;" : "=r"(u) : "r"(b.w[k].x & 0x7FFF7FFFu), "r"(b.w[k].y & 0x7FFF7FFFu));
+        asm("max.u16x2 %0, %1, %2;" : "=r"(v) : "r"(b.w[k].z & 0x7FFF7FFFu), "r"(b.w[k].w & 0x7FFF7FFFu));
+        asm("max.u16x2 %0, %1, %2;" : "=r"(t[k]) : "r"(u), "r"(v));
     }
-    publish_tensor_amax(a, m, false);
+    uint32_t m;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(t[0]), "r"(t[1]));
+    return max(m & 0xFFFFu, m >> 16) << 16;
 }
 
-// RHT blocks along rows.  Each CTA scans one contiguous range of blocks; a
-// thread keeps kAmaxDepth blocks' loads in flight (consecutive blocks of its
-// range, 32 bytes each for bf16) and transforms them as they land.
-constexpr int kAmaxDepth = 1;
-
-template <typename T>
-__global__ void __launch_bounds__(256) k_amax_rht_row(const QArgs a) {
-    const uint32_t CS = (uint32_t)(a.cols >> 4);
-    const uint32_t n = (uint32_t)a.rows * CS;
-    const uint32_t span = blockDim.x * kAmaxDepth;  // blocks per CTA step
-    const uint32_t per = ((n + gridDim.x - 1) / gridDim.x + span - 1) / span * span;
-    const uint32_t b0 = blockIdx.x * per, b1 = min(n, b0 + per);
-    const T *x = static_cast<const T *>(a.x);
+__device__ __forceinline__ uint32_t block_max_bits(const RawBlock<float> &b) {
     uint32_t m = 0;
-    for (uint32_t base = b0; base < b1; base += span) {
-        RawBlock<T> raw[kAmaxDepth];
 #pragma unroll
-        for (int k = 0; k < kAmaxDepth; k++) {
-            const uint32_t i = base + k * blockDim.x + threadIdx.x;
-            if (i < b1) {
-                const uint32_t r = i / CS, j = i - r * CS;
-                load_raw(x + (int64_t)r * a.ld + 16 * j, raw[k]);
-            }
+    for (int k = 0; k < 4; k++)
+        m = max(m, max(max(b.w[k].x & 0x7FFFFFFFu, b.w[k].y & 0x7FFFFFFFu),
+                       max(b.w[k].z & 0x7FFFFFFFu, b.w[k].w & 0x7FFFFFFFu)));
+    return m;
+}
+
+// Rowwise amax (and the plain amax of any orientation) through TMA: the CTA's
+// tiles of 128 rows x 64 columns (round robin) stream through kStreamStages
+// shared-memory stages, so tens of KB per SM are in flight while the threads
+// transform and reduce; thread t takes tile row t % 128 and blocks 2h, 2h+1
+// (h = t / 128).  Columns or rows past the edge arrive as zeros, which change
+// no maximum (and whose butterfly is zero).
+constexpr int kAmaxTmaThreads = 256;
+
+template <bool RHT, typename T>
+__global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_constant__ CUtensorMap tmap,
+                                                              const QArgs a) {
+    using ST = StreamTile<T>;
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ __align__(8) uint64_t full[kStreamStages];
+    __shared__ __align__(8) uint64_t empty[kStreamStages];
+    uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
+    const uint32_t ntc = (uint32_t)((a.cols + kStreamTileCols - 1) / kStreamTileCols);
+    const uint32_t ntiles = ntc * (uint32_t)((a.rows + kStreamTileRows - 1) / kStreamTileRows), G = gridDim.x;
+    const uint32_t nk = blockIdx.x < ntiles ? (ntiles - blockIdx.x + G - 1) / G : 0;
+    const int tid = threadIdx.x, trow = tid % kStreamTileRows, jb = (tid / kStreamTileRows) * 2;
+    auto issue = [&](uint32_t k) {
+        const uint32_t t = blockIdx.x + k * G, s = k % kStreamStages;
+        stream_issue<T>(&tmap, stages + s * ST::kStageBytes, &full[s], t / ntc, t % ntc);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kStreamStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kAmaxTmaThreads / 32);
         }
-#pragma unroll
-        for (int k = 0; k < kAmaxDepth; k++) {
-            if (base + k * blockDim.x + threadIdx.x < b1) {
-                f2 v[8];
-                unpack(raw[k], v);
-                fwht16(v);
-                m = max(m, __float_as_uint(block_amax(v)));
-            }
-        }
+        mbar_init_fence();
+        for (uint32_t k = 0; k < nk && k < (uint32_t)kStreamStages; k++) issue(k);
     }
-    publish_tensor_amax(a, m, true);
+    __syncthreads();
+    bool ok = true;
+    uint32_t m = 0;
+    for (uint32_t k = 0; k < nk; ++k) {
+        const uint32_t s = k % kStreamStages;
+        ok &= mbar_wait(&full[s], (k / kStreamStages) & 1u);
+        const uint8_t *stage = stages + s * ST::kStageBytes;
+#pragma unroll
+        for (int b = 0; b < 2; b++) {
+            RawBlock<T> raw;
+            stream_block<T>(stage, trow, jb + b, raw);
+            if (RHT) {
+                f2 v[8];
+                unpack(raw, v);
+                fwht16(v);
+                m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+            } else {
+                m = max(m, block_max_bits(raw));
+            }
+        }
+        ok &= stream_release(empty, k, tid, k + kStreamStages < nk, [&](uint32_t) { issue(k + kStreamStages); });
+    }
+    if (!ok) {  // a bounded wait gave up: poison the published scale, do not hang
+        atomicAdd(&g_wait_timeouts, 1u);
+        m = 0x7FFFFFFFu;
+    }
+    publish_tensor_amax(a, m, RHT);
 }
 
 // RHT blocks along columns: a thread owns 16 rows x one 16-byte chunk.
@@ -222,19 +240,35 @@ static int grid_for(K kernel, int64_t work_items) {
     return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+template <bool RHT, typename T>
+static cudaError_t run_amax_tma(const QArgs &a, cudaStream_t s) {
+    auto k = k_amax_tma<RHT, T>;
+    constexpr int smem = StreamTile<T>::kSmemBytes;
+    static bool configured = false;  // one attribute call per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    CUtensorMap map;
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, StreamTile<T>::kBoxCols, kStreamTileRows))
+        return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAmaxTmaThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t tiles = ((a.rows + kStreamTileRows - 1) / kStreamTileRows) *
+                          ((a.cols + kStreamTileCols - 1) / kStreamTileCols);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    k<<<(int)(tiles < cap ? tiles : cap), kAmaxTmaThreads, smem, s>>>(map, a);
+    return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t run_amax_tensor(const QArgs &a, bool rht, bool col, cudaStream_t s) {
     constexpr int W = Chunk<T>::W;
-    if (!rht) {
-        auto k = k_amax_plain<T>;
-        k<<<grid_for(k, a.rows * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
-    } else if (!col) {
-        auto k = k_amax_rht_row<T>;
-        k<<<grid_for(k, a.rows * (a.cols >> 4)), 256, 0, s>>>(a);
-    } else {
-        auto k = k_amax_rht_col<T>;
-        k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
-    }
+    if (!col) return rht ? run_amax_tma<true, T>(a, s) : run_amax_tma<false, T>(a, s);
+    auto k = k_amax_rht_col<T>;
+    k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

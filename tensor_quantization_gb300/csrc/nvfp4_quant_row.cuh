@@ -21,6 +21,7 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tiles.cuh"
 #include "nvfp4_tma.cuh"
 
 namespace nvfp4 {
@@ -246,46 +247,9 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
 // (Larger tensors run the amax and quantize kernels, whose second launch
 // overlaps the first's tail; there the one-kernel form gains nothing.)
 constexpr int kFusedThreads = 256;
-constexpr int kFusedTileRows = 128;
-constexpr int kFusedStages = 3;
+constexpr int kFusedTileRows = kStreamTileRows;
+constexpr int kFusedStages = kStreamStages;
 constexpr uint32_t kMaxGridPolls = 1u << 24;  // x >= 64 ns: the grid barrier gives up after ~1 s
-
-template <typename T>
-struct FusedTile {
-    static constexpr int kBoxCols = 128 / (int)sizeof(T);
-    static constexpr int kBoxes = kTileCols / kBoxCols;  // column boxes: 1 (bf16) or 2 (fp32)
-    static constexpr int kBoxBytes = kFusedTileRows * 128;
-    static constexpr int kStageBytes = kBoxes * kBoxBytes;
-    static constexpr int kSmemBytes = kFusedStages * kStageBytes + 1024;
-};
-
-template <typename T>
-__device__ __forceinline__ void fused_stage_block(const uint8_t *stage, int row, int b, RawBlock<T> &raw) {
-    constexpr int kChunks = (int)sizeof(T);
-    constexpr int kPerBoxRow = 8 / kChunks;
-    const uint8_t *base = stage + (b / kPerBoxRow) * FusedTile<T>::kBoxBytes + row * 128;
-#pragma unroll
-    for (int k = 0; k < kChunks; k++) {
-        const int c = (b % kPerBoxRow) * kChunks + k;
-        raw.w[k] = *reinterpret_cast<const uint4 *>(base + ((c ^ (row & 7)) << 4));
-    }
-}
-
-template <typename T>
-__device__ __forceinline__ void fused_issue(const CUtensorMap *map, uint8_t *stage, uint64_t *bar, uint32_t tr,
-                                            uint32_t tc) {
-    using FT = FusedTile<T>;
-    mbar_arrive_expect_tx(bar, FT::kStageBytes);
-#pragma unroll
-    for (int b = 0; b < FT::kBoxes; b++)
-        tma_load_2d(stage + b * FT::kBoxBytes, map, (int32_t)(tc * kTileCols + b * FT::kBoxCols),
-                    (int32_t)(tr * kFusedTileRows), bar);
-}
-
-// One arrival on a stage's release barrier.
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 
 // Thread 0 of every CTA: fold the CTA maximum (magnitude bits) into the
 // tensor maximum (ws[0]), count the CTA in (ws[1], ordered after the maximum
@@ -315,28 +279,11 @@ __device__ __forceinline__ bool grid_amax_barrier(uint32_t *ws, uint32_t m, uint
     return ok;
 }
 
-// Every warp releases load L (stage L % kFusedStages) after reading it;
-// thread 0 then waits for all warps and, if `more`, refills the stage through
-// refill(stage index).
-template <typename F>
-__device__ __forceinline__ bool fused_release(uint64_t *empty, uint32_t L, int tid, bool more, F &&refill) {
-    const uint32_t s = L % kFusedStages;
-    __syncwarp();
-    if ((tid & 31) == 0) mbar_arrive(&empty[s]);
-    bool ok = true;
-    if (tid == 0 && more) {
-        ok = mbar_wait(&empty[s], (L / kFusedStages) & 1u);
-        fence_async_shared();
-        refill(s);
-    }
-    return ok;
-}
-
 template <int MODE, bool RHT, typename T, bool AP>
 __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_constant__ CUtensorMap tmap,
                                                                   const QArgs a) {
     constexpr int NT = kFusedThreads, TR = kFusedTileRows;
-    using FT = FusedTile<T>;
+    using FT = StreamTile<T>;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ DivTable tab;
     __shared__ RhtMult rm;
@@ -353,7 +300,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
     // load L (0 <= L < 2 nk) is the CTA's tile L % nk: pass 1, then pass 2
     auto issue = [&](uint32_t L) {
         const uint32_t t = blockIdx.x + (L % nk) * G, s = L % kFusedStages;
-        fused_issue<T>(&tmap, stages + s * FT::kStageBytes, &full[s], t / ntc, t % ntc);
+        stream_issue<T>(&tmap, stages + s * FT::kStageBytes, &full[s], t / ntc, t % ntc);
     };
     if (tid == 0) {
         for (int s = 0; s < kFusedStages; s++) {
@@ -376,14 +323,14 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
 #pragma unroll
         for (int b = 0; b < 2; b++) {
             RawBlock<T> raw;
-            fused_stage_block<T>(stage, trow, jb + b, raw);  // past the edge: zeros
+            stream_block<T>(stage, trow, jb + b, raw);  // past the edge: zeros
             f2 v[8];
             unpack(raw, v);
             if (RHT) fwht16(v);
             m = absmax_nan(m, block_amax(v));
         }
         // pass 2's first loads follow pass 1's last ones without a break
-        ok &= fused_release(empty, k, tid, k + kFusedStages < 2 * nk, [&](uint32_t) { issue(k + kFusedStages); });
+        ok &= stream_release(empty, k, tid, k + kFusedStages < 2 * nk, [&](uint32_t) { issue(k + kFusedStages); });
     }
 
     // ---------------- grid-wide amax
@@ -443,7 +390,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
 #pragma unroll
             for (int b = 0; b < 2; b++) {
                 RawBlock<T> raw;
-                fused_stage_block<T>(stage, trow, jb + b, raw);
+                stream_block<T>(stage, trow, jb + b, raw);
                 f2 v[8];
                 unpack(raw, v);
                 if (fast) {
@@ -480,7 +427,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
                 }
             }
         }
-        ok &= fused_release(empty, L, tid, L + kFusedStages < 2 * nk, [&](uint32_t) { issue(L + kFusedStages); });
+        ok &= stream_release(empty, L, tid, L + kFusedStages < 2 * nk, [&](uint32_t) { issue(L + kFusedStages); });
     }
     if (!ok) {  // a bounded wait gave up somewhere in this CTA: the output is not trustworthy
         atomicAdd(&g_wait_timeouts, 1u);
@@ -823,7 +770,7 @@ cudaError_t dispatch_row(const QArgs &a, int mode, bool rht, bool scaled_rows, c
 template <int MODE, bool RHT, typename T, bool AP>
 cudaError_t run_row_fused(const QArgs &a, cudaStream_t s) {
     auto k = k_quant_row_fused<MODE, RHT, T, AP>;
-    constexpr int smem = FusedTile<T>::kSmemBytes;
+    constexpr int smem = StreamTile<T>::kSmemBytes;
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -834,7 +781,7 @@ cudaError_t run_row_fused(const QArgs &a, cudaStream_t s) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kFusedThreads, smem) != cudaSuccess || per_sm < 1)
         return cudaErrorNotSupported;
     CUtensorMap map;
-    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, FusedTile<T>::kBoxCols, kFusedTileRows))
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, StreamTile<T>::kBoxCols, kFusedTileRows))
         return cudaErrorInvalidValue;
     const int64_t tiles = ((a.rows + kFusedTileRows - 1) / kFusedTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
     const int64_t cap = (int64_t)sm_count() * per_sm;
