@@ -672,3 +672,35 @@ def test_rht_round_trip_through_the_library():
     torch.cuda.synchronize()
     err = (back.cpu() - x).reshape(-1, 16).norm(dim=1)
     assert float((err <= 0.5 * x.reshape(-1, 16).norm(dim=1) + 1e-30).float().mean()) > 0.99
+
+
+@pytest.mark.slow
+def test_full_size_rht_both_orientations_and_groups():
+    """The headline activation (8192x4096) in both orientations with the RHT, and
+    as 8 row groups of uneven sizes, compared in row bands with the oracle."""
+    w = wl.WORKLOADS["act_rht_sr_8192x4096"]
+    x, mask = wl.make_input(w)
+    kw = dict(mode="sr", rht=True, rowwise=True, colwise=True, swizzled=False, sign_mask=mask, seed=1)
+    g = gpu_run(x, **kw)
+    for orient, R_out in (("row", 8192), ("col", 4096)):
+        okw = dict(kw, rowwise=orient == "row", colwise=orient == "col")
+        for r0, r1 in bands(R_out):
+            o = oracle_run(x, row_range=(r0, r1), **okw)
+            assert np.array_equal(g[f"codes_{orient}"][r0:r1], o[f"codes_{orient}"][r0:r1]), (orient, r0)
+            assert np.array_equal(g[f"scales_{orient}"].reshape(R_out, -1)[r0:r1],
+                                  o[f"scales_{orient}"].reshape(R_out, -1)[r0:r1])
+        idx = 0 if orient == "row" else 1
+        assert same_float_bits(g["amax"][idx:idx + 1], o["amax"])
+    offs = [0, 100, 1124, 1124, 4000, 4001, 6000, 7999, 8192]
+    q = nvfp4.quantize_grouped(to_device(x), torch.tensor(offs, dtype=torch.int64, device="cuda"), mode="rht_sr",
+                               sign_mask=mask, seed=1)
+    torch.cuda.synchronize()
+    xn = np_bits(x)
+    for gi in (0, 1, 4, 6):
+        o0, o1 = offs[gi], offs[gi + 1]
+        A, _ = oracle.amax(xn[o0:o1], rht=True, sign_mask=mask)
+        r1 = min(o1, o0 + 64)
+        o = oracle.quantize(xn, mode="sr", rht=True, sign_mask=mask, seed=1, row_range=(o0, r1),
+                            amax_given=float(np.asarray(A).ravel()[0]))
+        assert np.array_equal(q.codes_row[o0:r1].cpu().numpy(), o["codes"][o0:r1]), gi
+        assert same_float_bits(q.amax[gi:gi + 1].cpu().numpy(), np.asarray(A).ravel())
