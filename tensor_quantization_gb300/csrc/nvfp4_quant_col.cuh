@@ -23,20 +23,23 @@ namespace {  // internal linkage: each including unit has its own kernels
 // arrive by TMA (128-byte swizzle) into one of two stages.  Thread t reads the
 // 8-byte half chunk hc = t % 16 of the 16 rows of row block rbl = t / 16 and
 // encodes the HC columns in it: each is one 16-element block of an X^T row.
-// Codes and scales go to a shared-memory output tile first (16 row blocks x
+// Codes and scales go to a shared-memory output tile first (RBT row blocks x
 // 8 bytes per output row, slots XOR-swizzled so the writes do not collide in
-// a bank), then out to global memory as 16-byte rows pieces, so every output
-// row gets 128 contiguous bytes per tile.
-constexpr int kColTileRows = 256;
-constexpr int kColStageBytes = kColTileRows * 128;
-
-template <typename T>
+// a bank), then out to global memory as 16-byte pieces, so every output row
+// gets RBT x 8 contiguous bytes per tile.  A tile has RBT row blocks and the
+// CTA 16 x RBT threads (RBT = 16 for both kernels: 128-row tiles with five
+// CTAs per SM measured a better median but a worse mean on the 2D workload).
+template <typename T, int RBT>
 struct ColTile {
+    static constexpr int TR = 16 * RBT;               // X rows per tile
+    static constexpr int NT = 16 * RBT;               // threads per CTA
     static constexpr int TC = 128 / (int)sizeof(T);  // X columns per tile
     static constexpr int HC = 8 / (int)sizeof(T);    // X columns per thread
-    static constexpr int kCodeBytes = TC * 128;      // output tile: TC rows x 16 blocks x 8 bytes
-    static constexpr int kScaleBytes = TC * 16;
-    static constexpr int kSmemBytes = 2 * (kColStageBytes + kCodeBytes + kScaleBytes) + 1024;
+    static constexpr int kStageBytes = TR * 128;
+    static constexpr int kPitch = RBT * 8;            // output tile: TC rows x RBT blocks x 8 bytes
+    static constexpr int kCodeBytes = TC * kPitch;
+    static constexpr int kScaleBytes = TC * RBT;
+    static constexpr int kSmemBytes = 2 * (kStageBytes + kCodeBytes + kScaleBytes) + 1024;
 };
 
 // Column cc (0..HC-1) of a thread's 16 x 8-byte strip as block pairs.
@@ -56,21 +59,24 @@ __device__ __forceinline__ void strip_block(const uint2 (&w)[16], int cc, f2 (&v
 }
 
 // Writes a staged output tile of the columnwise layout: output rows
-// o0..o0+TC-1, row blocks rb0..rb0+15 (codes as 16-byte pieces, scales as
-// words; narrower stores where alignment or the tensor edge requires).
-template <typename T>
+// o0..o0+TC-1, row blocks rb0..rb0+RBT-1 (codes as 16-byte pieces, scales as
+// words; narrower stores where alignment or the tensor edge requires).  Row
+// block rbl of output row ol sits in slot rbl ^ ((ol / HC) % RBT): the writing
+// thread's half chunk XOR-swizzles the slots.
+template <typename T, int RBT>
 __device__ __forceinline__ void write_col_tile(const QArgs &a, const uint8_t *ocs, const uint8_t *oss, uint32_t o0,
                                                uint32_t rb0, uint32_t C, uint32_t RB, uint32_t csp,
                                                int64_t code_pitch, bool codes16, bool words, bool lin_words,
                                                int tid) {
-    constexpr int TC = ColTile<T>::TC, HC = ColTile<T>::HC;
-    // codes: output row ol takes 8 pieces of 16 bytes (row blocks 2q, 2q+1)
-    for (int i = tid; i < TC * 8; i += 256) {
-        const int ol = i >> 3, q = i & 7;
+    using CT = ColTile<T, RBT>;
+    constexpr int TC = CT::TC, HC = CT::HC, NT = CT::NT, PIECES = RBT / 2, WORDS = RBT / 4;
+    // codes: output row ol takes RBT/2 pieces of 16 bytes (row blocks 2q, 2q+1)
+    for (int i = tid; i < TC * PIECES; i += NT) {
+        const int ol = i / PIECES, q = i % PIECES;
         const uint32_t o = o0 + ol, rba = rb0 + 2 * q;
         if (o >= C || rba >= RB) continue;
-        const int f = (ol / HC) & 15;
-        uint4 v = *reinterpret_cast<const uint4 *>(ocs + ol * 128 + (((2 * q) ^ (f & 14)) << 3));
+        const int f = (ol / HC) & (RBT - 1);
+        uint4 v = *reinterpret_cast<const uint4 *>(ocs + ol * CT::kPitch + (((2 * q) ^ (f & (RBT - 2))) << 3));
         if (f & 1) v = make_uint4(v.z, v.w, v.x, v.y);
         uint8_t *dst = a.codes_col + (int64_t)o * code_pitch + (int64_t)rba * 8;
         if (codes16 && rba + 1 < RB) {
@@ -80,9 +86,9 @@ __device__ __forceinline__ void write_col_tile(const QArgs &a, const uint8_t *oc
             if (rba + 1 < RB) *reinterpret_cast<uint2 *>(dst + 8) = make_uint2(v.z, v.w);
         }
     }
-    // scales: output row ol takes 4 words (row blocks 4q..4q+3)
-    for (int i = tid; i < TC * 4; i += 256) {
-        const int ol = i >> 2, q = i & 3;
+    // scales: output row ol takes RBT/4 words (row blocks 4q..4q+3)
+    for (int i = tid; i < TC * WORDS; i += NT) {
+        const int ol = i / WORDS, q = i % WORDS;
         const uint32_t o = o0 + ol, rbq = rb0 + 4 * q;
         if (o >= C || rbq >= RB) continue;
         const uint32_t word = (uint32_t)oss[(4 * q) * TC + ol] | ((uint32_t)oss[(4 * q + 1) * TC + ol] << 8) |
@@ -109,17 +115,18 @@ __device__ __forceinline__ void write_col_tile(const QArgs &a, const uint8_t *oc
 
 template <int MODE, bool RHT, typename T, bool AP>
 __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
-    using CT = ColTile<T>;
+    constexpr int RBT = 16;
+    using CT = ColTile<T, RBT>;
     constexpr int TC = CT::TC, HC = CT::HC;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ DivTable tab;
     __shared__ RhtMult rm;
     __shared__ __align__(8) uint64_t full[2];
     uint8_t *in = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
-    uint8_t *oc = in + 2 * kColStageBytes;
+    uint8_t *oc = in + 2 * CT::kStageBytes;
     uint8_t *os = oc + 2 * CT::kCodeBytes;
     const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, RB = R >> 4, csp = (RB + 3) & ~3u;
-    const uint32_t ntc = (C + TC - 1) / TC, ntr = (R + kColTileRows - 1) / kColTileRows;
+    const uint32_t ntc = (C + TC - 1) / TC, ntr = (R + CT::TR - 1) / CT::TR;
     const uint32_t ntiles = ntc * ntr;
     const int tid = threadIdx.x, hc = tid & 15, rbl = tid >> 4;
     if (tid == 0) {
@@ -128,9 +135,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CU
         for (int k = 0; k < 2; k++) {
             const uint32_t t = blockIdx.x + k * gridDim.x;
             if (t < ntiles) {
-                mbar_arrive_expect_tx(&full[k], kColStageBytes);
-                tma_load_2d(in + k * kColStageBytes, &tmap, (int32_t)((t % ntc) * TC),
-                            (int32_t)((t / ntc) * kColTileRows), &full[k]);
+                mbar_arrive_expect_tx(&full[k], CT::kStageBytes);
+                tma_load_2d(in + k * CT::kStageBytes, &tmap, (int32_t)((t % ntc) * TC),
+                            (int32_t)((t / ntc) * CT::TR), &full[k]);
             }
         }
     }
@@ -157,8 +164,8 @@ __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CU
             a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
         }
         const uint32_t tr = t / ntc, tc = t - tr * ntc;
-        const uint32_t rb0 = tr * 16, o0 = tc * TC, rb = rb0 + rbl;
-        const uint8_t *stage = in + s * kColStageBytes;
+        const uint32_t rb0 = tr * RBT, o0 = tc * TC, rb = rb0 + rbl;
+        const uint8_t *stage = in + s * CT::kStageBytes;
         uint8_t *ocs = oc + s * CT::kCodeBytes;
         uint8_t *oss = os + s * CT::kScaleBytes;
         uint2 w[16];
@@ -194,7 +201,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CU
                 }
             }
             // slot rbl of output row ol, XOR-swizzled by ol / HC (= hc)
-            *reinterpret_cast<uint2 *>(ocs + ol * 128 + ((rbl ^ hc) << 3)) = c;
+            *reinterpret_cast<uint2 *>(ocs + ol * CT::kPitch + ((rbl ^ (hc & (RBT - 1))) << 3)) = c;
             oss[rbl * TC + ol] = (uint8_t)S;
         }
         __syncthreads();  // output tile complete, stage s consumed
@@ -202,12 +209,12 @@ __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CU
             const uint32_t tn = t + 2 * gridDim.x;
             if (tn < ntiles) {
                 fence_async_shared();
-                mbar_arrive_expect_tx(&full[s], kColStageBytes);
-                tma_load_2d(in + s * kColStageBytes, &tmap, (int32_t)((tn % ntc) * TC),
-                            (int32_t)((tn / ntc) * kColTileRows), &full[s]);
+                mbar_arrive_expect_tx(&full[s], CT::kStageBytes);
+                tma_load_2d(in + s * CT::kStageBytes, &tmap, (int32_t)((tn % ntc) * TC),
+                            (int32_t)((tn / ntc) * CT::TR), &full[s]);
             }
         }
-        write_col_tile<T>(a, ocs, oss, o0, rb0, C, RB, csp, code_pitch, codes16, words, lin_words, tid);
+        write_col_tile<T, RBT>(a, ocs, oss, o0, rb0, C, RB, csp, code_pitch, codes16, words, lin_words, tid);
     }
 }
 
@@ -231,17 +238,18 @@ __device__ __forceinline__ f2 strip_pair(const uint2 &w, int p) {
 
 template <typename T, bool AP>
 __global__ void __launch_bounds__(256, 2) k_quant_2d(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
-    using CT = ColTile<T>;
+    constexpr int RBT = 16;
+    using CT = ColTile<T, RBT>;
     constexpr int TC = CT::TC, HC = CT::HC, NP = HC / 2, LPT = 16 / HC;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ DivTable tab;
     __shared__ __align__(8) uint64_t full[2];
     uint8_t *in = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
-    uint8_t *oc = in + 2 * kColStageBytes;
+    uint8_t *oc = in + 2 * CT::kStageBytes;
     uint8_t *os = oc + 2 * CT::kCodeBytes;
     const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, RB = R >> 4, CB = C >> 4;
     const uint32_t csp = (RB + 3) & ~3u, csp_row = (CB + 3) & ~3u;
-    const uint32_t ntc = (C + TC - 1) / TC, ntr = (R + kColTileRows - 1) / kColTileRows;
+    const uint32_t ntc = (C + TC - 1) / TC, ntr = (R + CT::TR - 1) / CT::TR;
     const uint32_t ntiles = ntc * ntr;
     const int tid = threadIdx.x, hc = tid & 15, rbl = tid >> 4, lane = tid & 31;
     if (tid == 0) {
@@ -250,9 +258,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_2d(const __grid_constant__ CUt
         for (int k = 0; k < 2; k++) {
             const uint32_t t = blockIdx.x + k * gridDim.x;
             if (t < ntiles) {
-                mbar_arrive_expect_tx(&full[k], kColStageBytes);
-                tma_load_2d(in + k * kColStageBytes, &tmap, (int32_t)((t % ntc) * TC),
-                            (int32_t)((t / ntc) * kColTileRows), &full[k]);
+                mbar_arrive_expect_tx(&full[k], CT::kStageBytes);
+                tma_load_2d(in + k * CT::kStageBytes, &tmap, (int32_t)((t % ntc) * TC),
+                            (int32_t)((t / ntc) * CT::TR), &full[k]);
             }
         }
     }
@@ -280,9 +288,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_2d(const __grid_constant__ CUt
             a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
         }
         const uint32_t tr = t / ntc, tc = t - tr * ntc;
-        const uint32_t rb0 = tr * 16, o0 = tc * TC, rb = rb0 + rbl, ob = o0 + HC * hc;
+        const uint32_t rb0 = tr * RBT, o0 = tc * TC, rb = rb0 + rbl, ob = o0 + HC * hc;
         const bool valid = rb < RB && ob < C;  // C % 16 == 0: a 16x16 tile is all in or all out
-        const uint8_t *stage = in + s * kColStageBytes;
+        const uint8_t *stage = in + s * CT::kStageBytes;
         uint8_t *ocs = oc + s * CT::kCodeBytes;
         uint8_t *oss = os + s * CT::kScaleBytes;
         uint2 w[16];
@@ -392,7 +400,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_2d(const __grid_constant__ CUt
 #pragma unroll
             for (int cc = 0; cc < HC; cc++) {
                 const int ol = HC * hc + cc;
-                *reinterpret_cast<uint2 *>(ocs + ol * 128 + ((rbl ^ hc) << 3)) = cw[cc];
+                *reinterpret_cast<uint2 *>(ocs + ol * CT::kPitch + ((rbl ^ (hc & (RBT - 1))) << 3)) = cw[cc];
                 oss[rbl * TC + ol] = (uint8_t)S;
             }
         }
@@ -401,30 +409,30 @@ __global__ void __launch_bounds__(256, 2) k_quant_2d(const __grid_constant__ CUt
             const uint32_t tn = t + 2 * gridDim.x;
             if (tn < ntiles) {
                 fence_async_shared();
-                mbar_arrive_expect_tx(&full[s], kColStageBytes);
-                tma_load_2d(in + s * kColStageBytes, &tmap, (int32_t)((tn % ntc) * TC),
-                            (int32_t)((tn / ntc) * kColTileRows), &full[s]);
+                mbar_arrive_expect_tx(&full[s], CT::kStageBytes);
+                tma_load_2d(in + s * CT::kStageBytes, &tmap, (int32_t)((tn % ntc) * TC),
+                            (int32_t)((tn / ntc) * CT::TR), &full[s]);
             }
         }
         if (a.want_col)
-            write_col_tile<T>(a, ocs, oss, o0, rb0, C, RB, csp, code_pitch, codes16, words, lin_words, tid);
+            write_col_tile<T, RBT>(a, ocs, oss, o0, rb0, C, RB, csp, code_pitch, codes16, words, lin_words, tid);
     }
 }
 
-// Persistent grid over the 256-row tiles (programmatic dependent launch: the
-// first tiles are staged while the amax pass finishes).
-template <typename K>
-cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, int smem, cudaStream_t s, int tc) {
+// Persistent grid over the tiles (programmatic dependent launch: the first
+// tiles are staged while the amax pass finishes).
+template <typename CT, typename K>
+cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, cudaStream_t s) {
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, CT::NT, CT::kSmemBytes);
     if (per_sm < 1) per_sm = 1;
-    const int64_t tiles = ((a.rows + kColTileRows - 1) / kColTileRows) * ((a.cols + tc - 1) / tc);
+    const int64_t tiles = ((a.rows + CT::TR - 1) / CT::TR) * ((a.cols + CT::TC - 1) / CT::TC);
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int grid = (int)(tiles < cap ? tiles : cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(CT::NT);
+    cfg.dynamicSmemBytes = CT::kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -437,7 +445,7 @@ cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, int smem, 
 template <int MODE, bool RHT, typename T, bool AP>
 cudaError_t run_col(const QArgs &a, cudaStream_t s) {
     auto k = k_quant_col<MODE, RHT, T, AP>;
-    constexpr int smem = ColTile<T>::kSmemBytes;
+    constexpr int smem = ColTile<T, 16>::kSmemBytes;
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -445,15 +453,15 @@ cudaError_t run_col(const QArgs &a, cudaStream_t s) {
         configured = true;
     }
     CUtensorMap map;
-    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, ColTile<T>::TC, kColTileRows))
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, ColTile<T, 16>::TC, ColTile<T, 16>::TR))
         return cudaErrorInvalidValue;
-    return launch_tiles(k, map, a, smem, s, ColTile<T>::TC);
+    return launch_tiles<ColTile<T, 16>>(k, map, a, s);
 }
 
 template <typename T, bool AP>
 cudaError_t run_2d(const QArgs &a, cudaStream_t s) {
     auto k = k_quant_2d<T, AP>;
-    constexpr int smem = ColTile<T>::kSmemBytes;
+    constexpr int smem = ColTile<T, 16>::kSmemBytes;
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -461,9 +469,9 @@ cudaError_t run_2d(const QArgs &a, cudaStream_t s) {
         configured = true;
     }
     CUtensorMap map;
-    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, ColTile<T>::TC, kColTileRows))
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, ColTile<T, 16>::TC, ColTile<T, 16>::TR))
         return cudaErrorInvalidValue;
-    return launch_tiles(k, map, a, smem, s, ColTile<T>::TC);
+    return launch_tiles<ColTile<T, 16>>(k, map, a, s);
 }
 
 template <typename T, bool AP>

@@ -553,7 +553,7 @@ __device__ __forceinline__ uint32_t row_bits_max(const uint8_t *rowp, uint32_t w
     }
 }
 
-template <int MODE, bool RHT, typename T, bool AP>
+template <int MODE, bool RHT, typename T, bool AP, bool GROUPED>
 __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, uint32_t buf_bytes) {
     extern __shared__ uint8_t dyn_smem[];
     __shared__ RowTables tabs[2];
@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
         const uint8_t *rowp = bufs + s * buf_bytes;
         // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max);
         // grouped scaling instead reads the final amax of the row's group
-        const bool grouped = a.n_groups > 0;
+        constexpr bool grouped = GROUPED;
         if (grouped && tid == 0) group_amax[par] = a.amax[group_of(a, r)];
         uint32_t mb = 0;
         if (grouped) {
@@ -723,9 +723,9 @@ cudaError_t run_row(const QArgs &a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, k, map, a);
 }
 
-template <int MODE, bool RHT, typename T, bool AP>
+template <int MODE, bool RHT, typename T, bool AP, bool GROUPED>
 cudaError_t run_rowscaled_staged(const QArgs &a, cudaStream_t s) {
-    auto k = k_quant_rowscaled_staged<MODE, RHT, T, AP>;
+    auto k = k_quant_rowscaled_staged<MODE, RHT, T, AP, GROUPED>;
     const uint32_t buf = ((uint32_t)(a.cols * sizeof(T)) + 15u) & ~15u;
     const int smem = (int)(kRowBufs * buf + 16);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -743,7 +743,12 @@ cudaError_t run_rowscaled_staged(const QArgs &a, cudaStream_t s) {
 
 template <int MODE, bool RHT, typename T, bool AP>
 cudaError_t run_rowscaled(const QArgs &a, cudaStream_t s) {
-    if ((uint64_t)a.cols * sizeof(T) <= kMaxStagedRowBytes) return run_rowscaled_staged<MODE, RHT, T, AP>(a, s);
+    if ((uint64_t)a.cols * sizeof(T) <= kMaxStagedRowBytes) {
+        if constexpr (!AP) {  // row groups (always exact quotients)
+            if (a.n_groups > 0) return run_rowscaled_staged<MODE, RHT, T, false, true>(a, s);
+        }
+        return run_rowscaled_staged<MODE, RHT, T, AP, false>(a, s);
+    }
     auto k = k_quant_rowscaled<MODE, RHT, T>;
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0);
