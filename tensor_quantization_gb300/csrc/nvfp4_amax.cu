@@ -72,6 +72,8 @@ __device__ __forceinline__ uint32_t block_max_bits(const RawBlock<float> &b) {
 // (h = t / 128).  Columns or rows past the edge arrive as zeros, which change
 // no maximum (and whose butterfly is zero).
 constexpr int kAmaxTmaThreads = 256;
+// two threads per tile row, two of its four blocks each
+static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "amax thread layout");
 
 template <bool RHT, typename T>
 __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_constant__ CUtensorMap tmap,

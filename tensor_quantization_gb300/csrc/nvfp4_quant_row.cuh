@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
 constexpr int kFusedThreads = 256;
 constexpr int kFusedTileRows = kStreamTileRows;
 constexpr int kFusedStages = kStreamStages;
+// two threads per tile row, two of its four blocks each
+static_assert(kFusedThreads == 2 * kFusedTileRows && kStreamTileCols == 64, "one-kernel thread layout");
 constexpr uint32_t kMaxGridPolls = 1u << 24;  // x >= 64 ns: the grid barrier gives up after ~1 s
 
 // Thread 0 of every CTA: fold the CTA maximum (magnitude bits) into the
