@@ -190,6 +190,14 @@ def aggregate_gbs(bytes_per_rank_step: int, ms_per_step: float, world: int) -> f
 
 
 # ----------------------------------------------------------- our arm
+def bench_config(w: wl.Workload, world: int) -> dict:
+    """The workload description both arms report."""
+    return {"workload": w.name, "rows": w.rows, "cols": w.cols, "input": "bf16", "mode": w.mode, "rht": w.rht,
+            "scales": "swizzled_32x4x4" if w.swizzled else "linear",
+            "l2": "flushed before every timed step: 512 MiB write + 256 MiB read",
+            "parallelism": f"replicas{world}" if world > 1 else "single_gpu"}
+
+
 def run_ours(args, rank: int, world: int) -> dict | None:
     from tensor_quantization_gb300 import build, nvfp4
 
@@ -346,10 +354,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "rows": R, "cols": C, "input": "bf16", "mode": w.mode, "rht": w.rht,
-                   "scales": "swizzled_32x4x4" if w.swizzled else "linear",
-                   "l2": "flushed before every timed step: 512 MiB write + 256 MiB read",
-                   "parallelism": f"replicas{world}" if world > 1 else "single_gpu"},
+        "config": bench_config(w, world),
         "counted_bytes_per_step": nbytes["total"],
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": roofline,
@@ -453,8 +458,7 @@ def run_reference(args) -> dict:
     return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "input": "bf16", "mode": w.mode,
-                       "rht": w.rht, "sample_rows": rows},
+            "config": bench_config(w, 1),
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
