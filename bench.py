@@ -485,7 +485,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, rank, world)
     if rank == 0:
-        if args.cpu_seconds > 0:
+        if args.cpu_seconds > 0 and world == 1:  # the CPU baseline is an N=1 figure
             w = workload_of(args)
             x_cpu, mask = wl.make_input(w)
             res["cpu_baseline"] = cpu_baseline(w, x_cpu, mask, args.cpu_seconds)
