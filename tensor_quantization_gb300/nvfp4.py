@@ -221,16 +221,22 @@ class Quantized:
 
 
 class Workspace:
-    """A zeroed workspace per device (reusable by calls on one stream)."""
-    _per_device: dict = {}
+    """A zeroed workspace per (device, stream): calls on one stream are ordered,
+    calls on different streams get different workspaces and may overlap."""
+    _cache: dict = {}
 
     @classmethod
-    def get(cls, device) -> torch.Tensor:
+    def get(cls, device, stream=None) -> torch.Tensor:
         dev = torch.device(device)
-        ws = cls._per_device.get(dev)
+        if dev.index is None:
+            dev = torch.device(dev.type, torch.cuda.current_device())
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        key = (dev, stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
+        ws = cls._cache.get(key)
         if ws is None:
             ws = torch.zeros(nvfp4_workspace_bytes(), dtype=torch.uint8, device=dev)
-            cls._per_device[dev] = ws
+            cls._cache[key] = ws
         return ws
 
 
@@ -264,7 +270,7 @@ def quantize(x: torch.Tensor, *, mode: str = "rne", rowwise: bool = True, colwis
     if amax is not None:
         q.amax.copy_(amax)
     o = make_output(q.codes_row, q.scales_row, q.codes_col, q.scales_col, q.amax, q.global_scale)
-    ws = Workspace.get(x.device)
+    ws = Workspace.get(x.device, stream)
     xin = make_input(x, row0, col0)
     with torch.cuda.device(x.device):
         if rht:

@@ -704,3 +704,23 @@ def test_full_size_rht_both_orientations_and_groups():
                             amax_given=float(np.asarray(A).ravel()[0]))
         assert np.array_equal(q.codes_row[o0:r1].cpu().numpy(), o["codes"][o0:r1]), gi
         assert same_float_bits(q.amax[gi:gi + 1].cpu().numpy(), np.asarray(A).ravel())
+
+
+def test_calls_on_two_streams_at_once():
+    """Two per-tensor quantizations in flight on two streams (each stream has its
+    own workspace in the binding) give the same results as one after the other."""
+    xa, xb = mixed_input(4096, 2048, seed=31), mixed_input(4096, 2048, seed=32)
+    da, db = to_device(xa), to_device(xb)
+    kw = dict(mode="sr", rht=True, sign_mask=0x1111, seed=9, swizzled=True)
+    ra, rb = gpu_run(xa, x_dev=da, **kw), gpu_run(xb, x_dev=db, **kw)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            qa = nvfp4.quantize(da, stream=s1, **kw)
+        with torch.cuda.stream(s2):
+            qb = nvfp4.quantize(db, stream=s2, **kw)
+        torch.cuda.synchronize()
+        assert np.array_equal(qa.codes_row.cpu().numpy(), ra["codes_row"])
+        assert np.array_equal(qb.codes_row.cpu().numpy(), rb["codes_row"])
+        assert same_float_bits(qa.amax.cpu().numpy(), ra["amax"]) and same_float_bits(qb.amax.cpu().numpy(), rb["amax"])
