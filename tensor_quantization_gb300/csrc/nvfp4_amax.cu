@@ -3,11 +3,9 @@
 // Per tensor: rowwise blocks (and the plain maximum of any orientation) are
 // streamed through shared memory by TMA; columnwise RHT blocks are read as
 // 16-row strips.  Magnitude-bit maximum per thread, warp (redux.sync) and CTA
-// trees, then ONE atomicMax per CTA into the workspace.  The CTA that takes the last ticket publishes amax and
-// g = amax / 2688 and returns the workspace to zero, so the pass needs no
-// memset and no second launch.  The host never waits: the per-tensor scale
-// stays on the device ("nvfp4-sm120" README, section "Results": the amax host
-// sync was 86% of the quantizer's time).
+// trees, then one reduction per CTA into the workspace; the result reaches
+// the quantize kernel, or the caller of the standalone entry point, as
+// nvfp4_tensor_amax.cuh describes.  No memset, no second launch, no host sync.
 //
 // With the RHT the maximum is over the post-transform magnitudes.  Signs do
 // not change magnitudes and rounding is monotone, so the kernel takes the
@@ -15,30 +13,11 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tensor_amax.cuh"
 #include "nvfp4_tiles.cuh"
 #include "nvfp4_tma.cuh"
 
 namespace nvfp4 {
-
-__device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, bool rht) {
-    __shared__ uint32_t red[32];
-    allow_dependents();  // the quantize pass may start staging its tiles
-    m = block_max_u32(m, red);
-    if (threadIdx.x == 0) {
-        atomicMax(&a.workspace[0], m);
-        __threadfence();
-        const uint32_t ticket = atomicAdd(&a.workspace[1], 1u);
-        if (ticket == gridDim.x - 1) {
-            __threadfence();
-            const uint32_t bits = atomicExch(&a.workspace[0], 0u);
-            atomicExch(&a.workspace[1], 0u);
-            float A = __uint_as_float(bits);
-            if (rht) A = __fmul_rn(A, 0.25f);
-            a.amax[0] = A;
-            a.gscale[0] = global_scale_of(A);
-        }
-    }
-}
 
 // Unsigned maximum of the magnitude bits of a raw block (bf16: two 16-bit
 // lanes per word, compared as integers; NaN patterns sort above +inf).
@@ -75,7 +54,7 @@ constexpr int kAmaxTmaThreads = 256;
 // two threads per tile row, two of its four blocks each
 static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "amax thread layout");
 
-template <bool RHT, typename T>
+template <bool RHT, typename T, bool PUBLISH>
 __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_constant__ CUtensorMap tmap,
                                                               const QArgs a) {
     using ST = StreamTile<T>;
@@ -125,11 +104,12 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
         atomicAdd(&g_wait_timeouts, 1u);
         m = 0x7FFFFFFFu;
     }
-    publish_tensor_amax(a, m, RHT);
+    if (PUBLISH) publish_tensor_amax(a, m, RHT);
+    else fold_tensor_amax(a, m);
 }
 
 // RHT blocks along columns: a thread owns 16 rows x one 16-byte chunk.
-template <typename T>
+template <typename T, bool PUBLISH>
 __global__ void __launch_bounds__(256) k_amax_rht_col(const QArgs a) {
     constexpr int CW = Chunk<T>::W;
     const uint32_t C = (uint32_t)a.cols;
@@ -154,7 +134,8 @@ __global__ void __launch_bounds__(256) k_amax_rht_col(const QArgs a) {
             m = max(m, __float_as_uint(block_amax(v)));
         }
     }
-    publish_tensor_amax(a, m, true);
+    if (PUBLISH) publish_tensor_amax(a, m, true);
+    else fold_tensor_amax(a, m);
 }
 
 // Per-row amax of the rowwise orientation: a CTA per row.
@@ -242,9 +223,9 @@ static int grid_for(K kernel, int64_t work_items) {
     return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
-template <bool RHT, typename T>
+template <bool RHT, typename T, bool PUBLISH>
 static cudaError_t run_amax_tma(const QArgs &a, cudaStream_t s) {
-    auto k = k_amax_tma<RHT, T>;
+    auto k = k_amax_tma<RHT, T, PUBLISH>;
     constexpr int smem = StreamTile<T>::kSmemBytes;
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
@@ -265,17 +246,18 @@ static cudaError_t run_amax_tma(const QArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool PUBLISH>
 static cudaError_t run_amax_tensor(const QArgs &a, bool rht, bool col, cudaStream_t s) {
     constexpr int W = Chunk<T>::W;
-    if (!col) return rht ? run_amax_tma<true, T>(a, s) : run_amax_tma<false, T>(a, s);
-    auto k = k_amax_rht_col<T>;
+    if (!col) return rht ? run_amax_tma<true, T, PUBLISH>(a, s) : run_amax_tma<false, T, PUBLISH>(a, s);
+    auto k = k_amax_rht_col<T, PUBLISH>;
     k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_amax_tensor(const QArgs &a, bool fp32, bool rht, bool col, cudaStream_t s) {
-    return fp32 ? run_amax_tensor<float>(a, rht, col, s) : run_amax_tensor<bf16_t>(a, rht, col, s);
+cudaError_t launch_amax_tensor(const QArgs &a, bool fp32, bool rht, bool col, bool publish, cudaStream_t s) {
+    if (publish) return fp32 ? run_amax_tensor<float, true>(a, rht, col, s) : run_amax_tensor<bf16_t, true>(a, rht, col, s);
+    return fp32 ? run_amax_tensor<float, false>(a, rht, col, s) : run_amax_tensor<bf16_t, false>(a, rht, col, s);
 }
 
 template <bool RHT, typename T>

@@ -139,8 +139,11 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
         st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, mode, rht, s));
     } else {
         if (!given) {  // (both orientations with the RHT: the rowwise amax first)
-            st = cuda_status(nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col && !want_row, s));
+            // the next quantize kernel takes the amax from the workspace and
+            // publishes it; a second one reads the published amax[0]
+            st = cuda_status(nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col && !want_row, false, s));
             if (st != NVFP4_OK) return st;
+            a.amax_in_ws = 1;
         }
         if (block2d) {
             st = cuda_status(nvfp4::launch_quant_2d(a, fp32, s));
@@ -153,10 +156,13 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
             ac.gscale = out->global_scale + 1;
             ac.blk_base = base_col;
             st = cuda_status(nvfp4::launch_quant_row(ar, fp32, mode, rht, s));
-            if (st == NVFP4_OK && !given) st = cuda_status(nvfp4::launch_amax_tensor(ac, fp32, rht, true, s));
+            if (st == NVFP4_OK && !given) st = cuda_status(nvfp4::launch_amax_tensor(ac, fp32, rht, true, false, s));
             if (st == NVFP4_OK) st = cuda_status(nvfp4::launch_quant_col(ac, fp32, mode, rht, s));
         } else {
-            if (want_row) st = cuda_status(nvfp4::launch_quant_row(a, fp32, mode, rht, s));
+            if (want_row) {
+                st = cuda_status(nvfp4::launch_quant_row(a, fp32, mode, rht, s));
+                a.amax_in_ws = 0;
+            }
             if (st == NVFP4_OK && want_col) {
                 a.blk_base = base_col;
                 st = cuda_status(nvfp4::launch_quant_col(a, fp32, mode, rht, s));
@@ -209,7 +215,7 @@ nvfp4_status nvfp4_amax(const nvfp4_input *in, uint32_t flags, int use_rht, uint
     nvfp4::QArgs a = make_args(in, out, workspace, 0);
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
     if (per_row) return cuda_status(nvfp4::launch_amax_rows(a, fp32, use_rht != 0, s));
-    return cuda_status(nvfp4::launch_amax_tensor(a, fp32, use_rht != 0, col, s));
+    return cuda_status(nvfp4::launch_amax_tensor(a, fp32, use_rht != 0, col, true, s));
 }
 
 nvfp4_status nvfp4_quantize_rne(const nvfp4_input *in, uint32_t flags, nvfp4_output *out, void *workspace,

@@ -170,16 +170,23 @@ __device__ __forceinline__ float neg_quot_slow(float y, float d) {
 }
 
 // --------------------------------------------------- stochastic rounding
+// The dither of element e, (r + 0.5) * 2^8 for its random byte r = byte
+// (e & 3) of word (e >> 2): one PRMT puts the byte above a constant 0x80 byte.
+__device__ __forceinline__ uint32_t dither8(const uint4 &r, int e) {
+    const uint32_t w = (e >> 2) == 0 ? r.x : (e >> 2) == 1 ? r.y : (e >> 2) == 2 ? r.z : r.w;
+    return __byte_perm(0x80u, w, 0x1140u + 16u * (uint32_t)(e & 3));
+}
+
 // Scaling |q| < 8 by 2^-126 (rounding toward zero) puts the E2M1 grid at the
 // floats whose low 22 bits are zero, subnormal step 0.5 included; adding the
-// dither (r + 0.5) * 2^14 to the bits and truncating gives
+// dither (r + 0.5) * 2^14 (= dither8 << 6) to the bits and truncating gives
 //   up  <=>  (|q| - a)/(b - a) + (r + 0.5)/256 >= 1
 // (the truncation only drops bits below the 2^-13 step of the dither, which
 // cannot change a ">=" against it).  Returns the chosen grid value, signed.
-__device__ __forceinline__ f2 sr_round2(f2 q, uint32_t r0, uint32_t r1) {
+__device__ __forceinline__ f2 sr_round2(f2 q, uint32_t d0, uint32_t d1) {
     f2 z = mulrz2(q, f2{0x1p-126f, 0x1p-126f});
-    uint32_t t0 = (__float_as_uint(z.x) + ((r0 << 14) | 0x2000u)) & 0xFFC00000u;
-    uint32_t t1 = (__float_as_uint(z.y) + ((r1 << 14) | 0x2000u)) & 0xFFC00000u;
+    uint32_t t0 = ((d0 << 6) + __float_as_uint(z.x)) & 0xFFC00000u;
+    uint32_t t1 = ((d1 << 6) + __float_as_uint(z.y)) & 0xFFC00000u;
     return mul2(f2{__uint_as_float(t0), __uint_as_float(t1)}, f2{0x1p126f, 0x1p126f});
 }
 
@@ -231,13 +238,16 @@ __device__ __forceinline__ uint4 block_random(uint64_t seed, uint64_t offset, ui
 // Butterfly with strides 1, 2, 4, 8 (this order defines the rounding).  The
 // block is held as 8 pairs v[k] = (y[2k], y[2k+1]); the stride-1 stage works
 // inside a pair, the later stages on whole pairs with packed adds.
-__device__ __forceinline__ void fwht16(f2 (&v)[8]) {
+__device__ __forceinline__ void fwht16_first(f2 (&v)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         float a = v[k].x, b = v[k].y;
         v[k].x = __fadd_rn(a, b);
         v[k].y = __fsub_rn(a, b);
     }
+}
+
+__device__ __forceinline__ void fwht16_rest(f2 (&v)[8]) {
 #pragma unroll
     for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
@@ -249,6 +259,11 @@ __device__ __forceinline__ void fwht16(f2 (&v)[8]) {
             }
         }
     }
+}
+
+__device__ __forceinline__ void fwht16(f2 (&v)[8]) {
+    fwht16_first(v);
+    fwht16_rest(v);
 }
 
 // Per-pair multipliers (+-0.25) from the sign mask: bit j -> element j.

@@ -69,12 +69,6 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, const Divisor &dm,
     return e4m3_rn(fast ? quot_pos(amax_b, dm) : __fdiv_rn(amax_b, dm.d));
 }
 
-// Random byte of element e (byte e&3 of word e>>2).
-__device__ __forceinline__ uint32_t rbyte(const uint4 &r, int e) {
-    const uint32_t w = (e >> 2) == 0 ? r.x : (e >> 2) == 1 ? r.y : (e >> 2) == 2 ? r.z : r.w;
-    return (w >> (8 * (e & 3))) & 0xFFu;
-}
-
 // E2M1 codes of one block against divisor D (S != 0): exactly rounded
 // quotients (negated, see neg_quot2), stochastic rounding when SR, the RN
 // cast, and one XOR per 8 codes to restore the sign.  .x = elements 0..7.
@@ -90,7 +84,7 @@ __device__ __forceinline__ uint2 encode_codes(const f2 (&y)[8], const Divisor &D
     }
     if (SR) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], rbyte(rnd, 2 * k), rbyte(rnd, 2 * k + 1));
+        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], dither8(rnd, 2 * k), dither8(rnd, 2 * k + 1));
     }
     uint2 c;
     c.x = e2m1x8(nq[0].x, nq[0].y, nq[1].x, nq[1].y, nq[2].x, nq[2].y, nq[3].x, nq[3].y) ^ 0x88888888u;
@@ -193,7 +187,7 @@ __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32
     }
     if (SR) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], rbyte(rnd, 2 * k), rbyte(rnd, 2 * k + 1));
+        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], dither8(rnd, 2 * k), dither8(rnd, 2 * k + 1));
     }
     const uint32_t keep = S ? 0xFFFFFFFFu : 0u;
     uint2 c;
@@ -203,12 +197,14 @@ __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32
 }
 
 // One block on the fast path.  v holds the raw block (RHT: the butterfly is
-// applied here and the 0.25 / signs are folded as above).  AP (fast math)
-// replaces the exact element quotient by y * RN(1/d); block scales stay exact.
-template <int MODE, bool RHT, bool AP = false>
+// applied here and the 0.25 / signs are folded as above; STAGE1: v already
+// holds the butterfly's first stage).  AP (fast math) replaces the exact
+// element quotient by y * RN(1/d); block scales stay exact.
+template <int MODE, bool RHT, bool AP = false, bool STAGE1 = false>
 __device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &sd, const DivTable &T,
                                                    uint2 signs, const uint4 &rnd, uint32_t &S_out) {
-    if (RHT) fwht16(v);
+    if (RHT && !STAGE1) fwht16_first(v);
+    if (RHT) fwht16_rest(v);
     float am = block_amax(v);
     if (RHT) am = __fmul_rn(am, 0.25f);  // = max |y|: rounding is monotone
     if (MODE == MODE_4O6) {

@@ -30,6 +30,9 @@ struct QArgs {
     int swizzled;
     int want_row, want_col;
     int fast_math;  // element quotient as y * RN(1/d)
+    // the per-tensor amax comes from this call's amax pass through the
+    // workspace (the quantize kernel publishes it) instead of amax[0]
+    int amax_in_ws;
     // grouped rowwise scaling: n_groups row ranges [offs[g], offs[g+1]), each
     // with its own amax / global scale (amax[g] final before the encode)
     const int64_t *group_offsets;
@@ -46,12 +49,14 @@ bool make_tmap_2d(CUtensorMap *map, const void *x, int elem_bytes, int64_t rows,
 
 // ---- launchers (return cudaGetLastError() after the launch) ----
 // Per-tensor amax (optionally of RHT blocks along rows (col=0) or columns
-// (col=1)); writes a.amax[0], a.gscale[0] and resets the workspace.
-cudaError_t launch_amax_tensor(const QArgs &a, bool fp32, bool rht, bool col, cudaStream_t s);
+// (col=1)).  publish: writes a.amax[0], a.gscale[0] and resets the workspace;
+// otherwise leaves the maximum bits in the workspace for the quantize kernel
+// launched next with a.amax_in_ws set.
+cudaError_t launch_amax_tensor(const QArgs &a, bool fp32, bool rht, bool col, bool publish, cudaStream_t s);
 // Per-row amax of the rowwise orientation (one value per X row).
 cudaError_t launch_amax_rows(const QArgs &a, bool fp32, bool rht, cudaStream_t s);
 
-// Rowwise 1x16 quantize with a per-tensor scale (a.amax[0]).
+// Rowwise 1x16 quantize with a per-tensor scale (a.amax[0], or the workspace).
 cudaError_t launch_quant_row(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);
 // Columnwise 1x16 quantize with a per-tensor scale.
 cudaError_t launch_quant_col(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);

@@ -56,6 +56,27 @@ __device__ __forceinline__ void unpack(const RawBlock<float> &b, f2 (&v)[8]) {
     }
 }
 
+// Unpack a raw block and run the butterfly's first stage, (a, b) ->
+// (a + b, a - b) on each pair.  For bf16 the even element a enters the adds
+// as a bf16 operand of a mixed-precision add (it widens exactly, so the
+// result is the fp32 sum), which saves unpacking it.
+__device__ __forceinline__ void fwht_first_bf16(uint32_t w, f2 &o) {
+    const float b = bf16_hi(w);
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, lo, %3; sub.rn.f32.bf16 %1, lo, %3; }"
+        : "=f"(o.x), "=f"(o.y)
+        : "r"(w), "f"(b));
+}
+__device__ __forceinline__ void unpack_fwht_first(const RawBlock<bf16_t> &b, f2 (&v)[8]) {
+    fwht_first_bf16(b.w[0].x, v[0]); fwht_first_bf16(b.w[0].y, v[1]);
+    fwht_first_bf16(b.w[0].z, v[2]); fwht_first_bf16(b.w[0].w, v[3]);
+    fwht_first_bf16(b.w[1].x, v[4]); fwht_first_bf16(b.w[1].y, v[5]);
+    fwht_first_bf16(b.w[1].z, v[6]); fwht_first_bf16(b.w[1].w, v[7]);
+}
+__device__ __forceinline__ void unpack_fwht_first(const RawBlock<float> &b, f2 (&v)[8]) {
+    unpack(b, v);
+    fwht16_first(v);
+}
+
 // A 16-byte chunk of one row: 8 bf16 or 4 fp32 elements.  When fewer than a
 // full chunk of columns remain, the missing elements read as zero.
 template <typename T>

@@ -13,6 +13,7 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tensor_amax.cuh"
 #include "nvfp4_tma.cuh"
 
 namespace nvfp4 {
@@ -144,12 +145,13 @@ __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CU
     const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
     if (RHT) build_rht_mult(rm, a.sign_mask, tid);
     grid_dependency_wait();
-    const float g = global_scale_of(a.amax[0]);
+    const float A = tensor_amax_read(a, RHT);
+    const float g = global_scale_of(A);
     build_table(tab, g, tid, blockDim.x);
     const ScaleDiv sd = make_scale_div(g);
     const bool fast = scale_all_fast(g);
-    if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
     __syncthreads();
+    tensor_amax_done(a, A, g);
 
     const int64_t code_pitch = R >> 1;
     const bool codes16 = (code_pitch & 15) == 0 && (reinterpret_cast<uintptr_t>(a.codes_col) & 15u) == 0;
@@ -265,12 +267,13 @@ __global__ void __launch_bounds__(256, 2) k_quant_2d(const __grid_constant__ CUt
         }
     }
     grid_dependency_wait();
-    const float g = global_scale_of(a.amax[0]);
+    const float A = tensor_amax_read(a, false);
+    const float g = global_scale_of(A);
     build_table(tab, g, tid, blockDim.x);
     const ScaleDiv sd = make_scale_div(g);
     const bool fast = scale_all_fast(g);
-    if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
     __syncthreads();
+    tensor_amax_done(a, A, g);
 
     const int64_t code_pitch = R >> 1, row_pitch = C >> 1;
     const bool codes16 = (code_pitch & 15) == 0 && (reinterpret_cast<uintptr_t>(a.codes_col) & 15u) == 0;

@@ -21,6 +21,7 @@
 #include "nvfp4_encode.cuh"
 #include "nvfp4_internal.h"
 #include "nvfp4_load.cuh"
+#include "nvfp4_tensor_amax.cuh"
 #include "nvfp4_tiles.cuh"
 #include "nvfp4_tma.cuh"
 
@@ -130,12 +131,13 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
     const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
     if (RHT) build_rht_mult(rm, a.sign_mask, tid);
     grid_dependency_wait();
-    const float g = global_scale_of(a.amax[0]);
+    const float A = tensor_amax_read(a, RHT);
+    const float g = global_scale_of(A);
     build_table(tab, g, tid, blockDim.x);
     const ScaleDiv sd = make_scale_div(g);
     const bool fast = scale_all_fast(g);  // uniform: every divisor in the fast range
-    if (blockIdx.x == 0 && tid == 0) a.gscale[0] = g;
     __syncthreads();
+    tensor_amax_done(a, A, g);
 
     // vector stores only where every address is aligned for them
     const bool codes16 = (C & 31u) == 0 && (reinterpret_cast<uintptr_t>(a.codes_row) & 15u) == 0;
@@ -174,8 +176,9 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
                         RawBlock<T> raw;
                         stage_block<T>(stage, tid, b, raw);
                         f2 v[8];
-                        unpack(raw, v);
-                        c[b] = encode_block_fast<MODE, RHT, AP>(v, sd, tab, signs, rnd[b], S[b]);
+                        if (RHT) unpack_fwht_first(raw, v);
+                        else unpack(raw, v);
+                        c[b] = encode_block_fast<MODE, RHT, AP, true>(v, sd, tab, signs, rnd[b], S[b]);
                     }
                 }
             } else {

@@ -27,7 +27,7 @@ __global__ void k_e2m1_order(uint32_t *out) {
 __global__ void k_sr(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= n) return;
-    f2 v = sr_round2(f2{q[i], 0.f}, r[i], 0u);  // symmetric: also used on -q
+    f2 v = sr_round2(f2{q[i], 0.f}, dither8(make_uint4(r[i], 0u, 0u, 0u), 0), 0x80u);  // symmetric: also used on -q
     out[i] = (uint8_t)(e2m1x8(v.x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 15u);
 }
 
