@@ -44,12 +44,14 @@ __device__ __forceinline__ uint32_t block_max_bits(const RawBlock<float> &b) {
     return m;
 }
 
-// Rowwise amax (and the plain amax of any orientation) through TMA: the CTA's
-// tiles of 128 rows x 64 columns (round robin) stream through kStreamStages
-// shared-memory stages, so tens of KB per SM are in flight while the threads
-// transform and reduce; thread t takes tile row t % 128 and blocks 2h, 2h+1
-// (h = t / 128).  Columns or rows past the edge arrive as zeros, which change
-// no maximum (and whose butterfly is zero).
+// Rowwise amax (and the plain amax of any orientation) through TMA: tiles of
+// 128 rows x 64 columns stream through kStreamStages shared-memory stages per
+// CTA, so tens of KB per SM are in flight while the threads transform and
+// reduce; thread t takes tile row t % 128 and blocks 2h, 2h+1 (h = t / 128).
+// Tiles after the first kStreamStages of each CTA come from a TileQueue:
+// from the counter workspace[2] in the standalone pass, round robin in a
+// quantize call.  Columns or rows past the edge arrive as zeros, which change no
+// maximum (and whose butterfly is zero).
 constexpr int kAmaxTmaThreads = 256;
 // two threads per tile row, two of its four blocks each
 static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "amax thread layout");
@@ -61,29 +63,53 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full[kStreamStages];
     __shared__ __align__(8) uint64_t empty[kStreamStages];
+    __shared__ uint32_t stage_tile[kStreamStages];  // tile in the stage, or kNoTile: the stream ended
+    __shared__ uint32_t warp_max, warps_in;
     uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
     const uint32_t ntc = (uint32_t)((a.cols + kStreamTileCols - 1) / kStreamTileCols);
-    const uint32_t ntiles = ntc * (uint32_t)((a.rows + kStreamTileRows - 1) / kStreamTileRows), G = gridDim.x;
-    const uint32_t nk = blockIdx.x < ntiles ? (ntiles - blockIdx.x + G - 1) / G : 0;
+    const uint32_t ntiles = ntc * (uint32_t)((a.rows + kStreamTileRows - 1) / kStreamTileRows);
     const int tid = threadIdx.x, trow = tid % kStreamTileRows, jb = (tid / kStreamTileRows) * 2;
-    auto issue = [&](uint32_t k) {
-        const uint32_t t = blockIdx.x + k * G, s = k % kStreamStages;
-        stream_issue<T>(&tmap, stages + s * ST::kStageBytes, &full[s], t / ntc, t % ntc);
+    TileQueue q;  // thread 0's
+    // thread 0: put tile t (or the end of the stream) into stage s
+    auto fill = [&](uint32_t s, uint32_t t) {
+        stage_tile[s] = t;
+        if (t == kNoTile) {
+            mbar_arrive(&full[s]);
+        } else {
+            stream_issue<T>(&tmap, stages + s * ST::kStageBytes, &full[s], t / ntc, t % ntc);
+        }
     };
     if (tid == 0) {
         for (int s = 0; s < kStreamStages; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kAmaxTmaThreads / 32);
         }
+        warp_max = 0u;
+        warps_in = 0u;
         mbar_init_fence();
-        for (uint32_t k = 0; k < nk && k < (uint32_t)kStreamStages; k++) issue(k);
+        // dynamic tiles for the standalone pass, whose last CTA publishes (the
+        // CTAs then finish together: 1.8 us less on 8192x4096); in a quantize
+        // call static tiles measured faster (the quantize kernel's first CTAs
+        // start on SMs that finish early)
+        q.init(PUBLISH ? a.workspace + 2 : nullptr, ntiles, kStreamStages);
+        bool complete = true;
+        for (uint32_t k = 0; k < (uint32_t)kStreamStages && complete; k++) {
+            const uint32_t t = q.static_tile(k);
+            fill(k, t);
+            complete = t != kNoTile;
+        }
+        q.start(complete);
     }
     __syncthreads();
     bool ok = true;
     uint32_t m = 0;
-    for (uint32_t k = 0; k < nk; ++k) {
+    for (uint32_t k = 0;; ++k) {
         const uint32_t s = k % kStreamStages;
-        ok &= mbar_wait(&full[s], (k / kStreamStages) & 1u);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (k / kStreamStages) & 1u))) {  // warp-uniform exit
+            ok = false;
+            break;
+        }
+        if (*reinterpret_cast<volatile uint32_t *>(&stage_tile[s]) == kNoTile) break;
         const uint8_t *stage = stages + s * ST::kStageBytes;
 #pragma unroll
         for (int b = 0; b < 2; b++) {
@@ -98,14 +124,14 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
                 m = max(m, block_max_bits(raw));
             }
         }
-        ok &= stream_release(empty, k, tid, k + kStreamStages < nk, [&](uint32_t) { issue(k + kStreamStages); });
+        ok &= stream_release(empty, k, tid, tid == 0 && !q.done, [&](uint32_t st) { fill(st, q.next()); });
     }
     if (!ok) {  // a bounded wait gave up: poison the published scale, do not hang
         atomicAdd(&g_wait_timeouts, 1u);
         m = 0x7FFFFFFFu;
     }
     if (PUBLISH) publish_tensor_amax(a, m, RHT);
-    else fold_tensor_amax(a, m);
+    else fold_tensor_amax_warps(a, m, &warp_max, &warps_in);
 }
 
 // RHT blocks along columns: a thread owns 16 rows x one 16-byte chunk.

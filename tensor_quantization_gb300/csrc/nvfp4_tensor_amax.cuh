@@ -30,6 +30,24 @@ __device__ __forceinline__ void fold_tensor_amax(const QArgs &a, uint32_t m) {
     if (threadIdx.x == 0) asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a.workspace), "r"(m) : "memory");
 }
 
+// The same without a CTA barrier: each warp folds its maximum into a shared
+// word (zeroed before the CTA's first barrier) and the last warp to count in
+// sends the CTA's maximum, so no warp waits for another.
+__device__ __forceinline__ void fold_tensor_amax_warps(const QArgs &a, uint32_t m, uint32_t *cta_max,
+                                                       uint32_t *warps_in) {
+    allow_dependents();
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) {
+        atomicMax(cta_max, m);
+        __threadfence_block();
+        if (atomicAdd(warps_in, 1u) == blockDim.x / 32 - 1) {
+            __threadfence_block();
+            const uint32_t cm = *reinterpret_cast<volatile uint32_t *>(cta_max);
+            asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a.workspace), "r"(cm) : "memory");
+        }
+    }
+}
+
 // End of a standalone amax pass: the last CTA publishes amax and g and zeroes
 // the workspace.
 __device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, bool rht) {

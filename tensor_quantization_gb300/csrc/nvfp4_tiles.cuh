@@ -49,6 +49,72 @@ __device__ __forceinline__ void stream_issue(const CUtensorMap *map, uint8_t *st
                     (int32_t)(tr * kStreamTileRows), bar);
 }
 
+// Tiles handed to persistent CTAs.  Load k < `stages` of CTA b is the static
+// tile b + k * G (G CTAs); every later tile comes from a counter in global
+// memory, one atomicAdd per tile, requested one load ahead so that its
+// latency hides behind the stage being computed.  A CTA whose data arrives
+// late takes fewer tiles, so the CTAs finish together instead of waiting for
+// the slowest static share.  Every CTA makes exactly one request that finds
+// the tiles exhausted; the request that returns the counter's final value
+// (dynamic tiles + G - 1) is the last of the call and zeroes the counter for
+// the next one.  Without a counter (a call given no workspace) every tile is
+// static.  Used by thread 0 only.
+constexpr uint32_t kNoTile = 0xFFFFFFFFu;
+
+struct TileQueue {
+    uint32_t *ctr;
+    uint32_t ntiles, first_dyn, final_v, pending, k_static;
+    bool done;
+
+    __device__ __forceinline__ void init(uint32_t *counter, uint32_t n, uint32_t stages) {
+        ctr = counter;
+        ntiles = n;
+        first_dyn = stages * gridDim.x;
+        final_v = (n > first_dyn ? n - first_dyn : 0u) + gridDim.x - 1u;
+        pending = 0u;
+        k_static = stages;
+        done = false;
+    }
+    // Tile of static load k, or kNoTile.
+    __device__ __forceinline__ uint32_t static_tile(uint32_t k) const {
+        const uint32_t t = blockIdx.x + k * gridDim.x;
+        return t < ntiles ? t : kNoTile;
+    }
+    __device__ __forceinline__ void request() { pending = atomicAdd(ctr, 1u); }
+    // After the first `stages` static loads: request the first dynamic tile,
+    // or (if the static loads already ran out) make the CTA's one failing
+    // request now.
+    __device__ __forceinline__ void start(bool statics_complete) {
+        if (!ctr) {
+            done = !statics_complete;
+            return;
+        }
+        request();
+        if (!statics_complete) finish();
+    }
+    // The next tile (requesting the one after it), or kNoTile once the tiles
+    // are exhausted.
+    __device__ __forceinline__ uint32_t next() {
+        if (done) return kNoTile;
+        if (!ctr) {
+            const uint32_t t = static_tile(k_static++);
+            done = t == kNoTile;
+            return t;
+        }
+        const uint32_t t = first_dyn + pending;
+        if (t < ntiles) {
+            request();
+            return t;
+        }
+        finish();
+        return kNoTile;
+    }
+    __device__ __forceinline__ void finish() {
+        done = true;
+        if (pending == final_v) *reinterpret_cast<volatile uint32_t *>(ctr) = 0u;
+    }
+};
+
 // One arrival on a stage's release barrier.
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
