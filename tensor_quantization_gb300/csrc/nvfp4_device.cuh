@@ -124,10 +124,13 @@ __device__ __forceinline__ f2 e2m1x2_value(uint32_t b) {
 //                              Floating-Point Arithmetic, division chapter).
 // The sequence is evaluated on negated reciprocals and returns -q, which keeps
 // every signed zero exact without a sign fix-up; callers flip the code sign.
-// Fast-path precondition: d in [2^-80, 2^100], y finite.  Quotients below
-// 2^-11 may be inexact but stay below 2^-10 with the right sign, which fixes
-// their E2M1 code and their E4M3 rounding; a quotient that overflows becomes
-// +-inf, which both the saturating casts and sr_round2 encode as +-6.
+// Fast-path precondition: d in [2^-80, 2^100], y finite.  With |y| >= 2^-100
+// and |y/d| >= 2^-100 nothing underflows (t and rl err by far less than the
+// quotient's ulp, the remainder is representable, the result is normal), so
+// the result is exact.  Otherwise |y/d| < 2^-20 and the computed value stays
+// that small with the sign of y, which fixes its E2M1 code and its E4M3
+// rounding (both 0), also at the 2^-14 scale of sr_pair_f16; a quotient that
+// overflows becomes +-inf, which the saturating casts encode as +-6.
 struct Divisor {
     float d, nrh, nrd, nrl;  // d, -RN(1/d), -RD(1/d), -rl
 };
@@ -188,6 +191,46 @@ __device__ __forceinline__ f2 sr_round2(f2 q, uint32_t d0, uint32_t d1) {
     uint32_t t0 = ((d0 << 6) + __float_as_uint(z.x)) & 0xFFC00000u;
     uint32_t t1 = ((d1 << 6) + __float_as_uint(z.y)) & 0xFFC00000u;
     return mul2(f2{__uint_as_float(t0), __uint_as_float(t1)}, f2{0x1p126f, 0x1p126f});
+}
+
+// The same decision two elements at a time through fp16 (fast path).  The
+// divisor carries a factor 2^14, so the negated quotients arrive as
+// -q * 2^-14, exact (a power-of-two scaling of RN(y/d) in the normal range;
+// only |q| < 2^-112 could round differently, and every such q encodes as 0).
+// Converting the pair to f16x2 toward zero truncates each |q| * 2^-14 to a
+// multiple of 2^-10 grid steps: q = 1 is the smallest normal f16, so below it
+// the subnormal step holds the 0.5 grid step at bit 9, and above it each
+// binade keeps one mantissa bit above bit 9.  Adding 2r + 1 to each 16-bit
+// lane (the same dither (r + 0.5)/256 of a grid step; no carry leaves a lane)
+// and clearing the low 9 bits makes the same decision as sr_round2.  The grid
+// values times 2^14 (exact in f16) then go through the f16x2 -> e2m1x2 cast
+// (satfinite: 8 and 12 encode as 6).  Pair k holds elements 2k (low half) and
+// 2k + 1, whose random bytes are bytes 2k & 3 and (2k & 3) + 1 of word k / 2.
+__device__ __forceinline__ uint32_t sr_pair_f16(f2 nq, const uint4 &r, int k) {
+    uint32_t h;
+    asm("cvt.rz.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(nq.y), "f"(nq.x));
+    const uint32_t w = (k >> 1) == 0 ? r.x : (k >> 1) == 1 ? r.y : (k >> 1) == 2 ? r.z : r.w;
+    const uint32_t bb = (uint32_t)(2 * k) & 3u;
+    const uint32_t t = __byte_perm(w, 0u, 0x4040u | bb | ((bb + 1u) << 8));  // r_odd << 16 | r_even
+    const uint32_t m = (h + (t << 1) + 0x00010001u) & 0xFE00FE00u;
+    uint32_t o;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o) : "r"(m), "r"(0x74007400u));  // x 2^14
+    return o;
+}
+
+// Four f16x2 pairs -> eight RNE/satfinite E2M1 codes, element k in nibble k
+// (the high half of a pair is the high nibble of its byte).
+__device__ __forceinline__ uint32_t e2m1x8_f16(uint32_t h0, uint32_t h1, uint32_t h2, uint32_t h3) {
+    uint32_t w;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f16x2 b0, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f16x2 b1, %2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f16x2 b2, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f16x2 b3, %4;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(w)
+        : "r"(h0), "r"(h1), "r"(h2), "r"(h3));
+    return w;
 }
 
 // ----------------------------------------------------------- Philox4x32-10

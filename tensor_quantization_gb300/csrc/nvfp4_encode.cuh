@@ -158,8 +158,9 @@ __device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &
 // per-block range test.  With S != 0x7F guaranteed (the block amax is finite),
 // an all-zero block is the only special case and is masked to +0 codes.
 __device__ __forceinline__ bool scale_all_fast(float g) {
-    // smallest divisor 2^-9 * g, largest 448 * g (x4 for the folded RHT)
-    return g >= 0x1p-71f && g <= 0x1p89f;  // false for NaN
+    // smallest divisor 2^-9 * g, largest 448 * g (x 2^16 for the folded RHT
+    // and the fp16 stochastic rounding)
+    return g >= 0x1p-71f && g <= 0x1p73f;  // false for NaN
 }
 
 // The RHT's outputs are y_j = s_j * 0.25 * v'_j (v' = butterfly output).  On
@@ -171,11 +172,15 @@ __device__ __forceinline__ bool scale_all_fast(float g) {
 template <bool SR, bool AP = false>
 __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32_t S, bool fold4,
                                              uint2 signs, const uint4 &rnd) {
-    if (fold4) {
-        D.d = __fmul_rn(D.d, 4.0f);
-        D.nrh = __fmul_rn(D.nrh, 0.25f);
-        D.nrd = __fmul_rn(D.nrd, 0.25f);
-        D.nrl = __fmul_rn(D.nrl, 0.25f);
+    // the divisor's exact power-of-two factor: 4 for the folded RHT, 2^14
+    // for stochastic rounding through fp16 (sr_pair_f16)
+    const float up = SR ? (fold4 ? 0x1p16f : 0x1p14f) : (fold4 ? 4.0f : 1.0f);
+    const float dn = SR ? (fold4 ? 0x1p-16f : 0x1p-14f) : (fold4 ? 0.25f : 1.0f);
+    if (SR || fold4) {
+        D.d = __fmul_rn(D.d, up);
+        D.nrh = __fmul_rn(D.nrh, dn);
+        D.nrd = __fmul_rn(D.nrd, dn);
+        D.nrl = __fmul_rn(D.nrl, dn);
     }
     f2 nq[8];
     if (AP) {  // fast math: -(y * RN(1/d)), one multiply
@@ -185,12 +190,16 @@ __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32
 #pragma unroll
         for (int k = 0; k < 8; k++) nq[k] = neg_quot2(v[k], D);
     }
-    if (SR) {
-#pragma unroll
-        for (int k = 0; k < 8; k++) nq[k] = sr_round2(nq[k], dither8(rnd, 2 * k), dither8(rnd, 2 * k + 1));
-    }
     const uint32_t keep = S ? 0xFFFFFFFFu : 0u;
     uint2 c;
+    if (SR) {
+        uint32_t h[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) h[k] = sr_pair_f16(nq[k], rnd, k);
+        c.x = (e2m1x8_f16(h[0], h[1], h[2], h[3]) ^ 0x88888888u ^ signs.x) & keep;
+        c.y = (e2m1x8_f16(h[4], h[5], h[6], h[7]) ^ 0x88888888u ^ signs.y) & keep;
+        return c;
+    }
     c.x = (e2m1x8(nq[0].x, nq[0].y, nq[1].x, nq[1].y, nq[2].x, nq[2].y, nq[3].x, nq[3].y) ^ 0x88888888u ^ signs.x) & keep;
     c.y = (e2m1x8(nq[4].x, nq[4].y, nq[5].x, nq[5].y, nq[6].x, nq[6].y, nq[7].x, nq[7].y) ^ 0x88888888u ^ signs.y) & keep;
     return c;

@@ -31,6 +31,29 @@ __global__ void k_sr(const float *q, const uint8_t *r, int64_t n, uint8_t *out) 
     out[i] = (uint8_t)(e2m1x8(v.x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 15u);
 }
 
+// The fp16 stochastic-rounding pair on q * 2^-14 (as the scaled divisor
+// delivers it): element i is paired with a zero partner, alternately in the
+// low and the high half (random byte 0 or 1 of word 0), so both lanes and
+// both nibbles are checked.
+__global__ void k_sr_f16(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float qs = q[i] * 0x1p-14f;
+    const bool hi = i & 1;
+    const uint4 rw = make_uint4(hi ? (uint32_t)r[i] << 8 : (uint32_t)r[i], 0u, 0u, 0u);
+    const uint32_t h = sr_pair_f16(hi ? f2{0.f, qs} : f2{qs, 0.f}, rw, 0);
+    const uint32_t w = e2m1x8_f16(h, 0u, 0u, 0u);
+    out[i] = (uint8_t)((hi ? w >> 4 : w) & 15u);
+}
+
+// The f16x2 -> e2m1x2 cast on every f16 pattern (paired with +0), in both halves.
+__global__ void k_e2m1_f16(uint8_t *out) {
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;  // 0 .. 65535
+    const uint32_t lo = e2m1x8_f16(i, 0u, 0u, 0u) & 15u;
+    const uint32_t hi = (e2m1x8_f16(i << 16, 0u, 0u, 0u) >> 4) & 15u;
+    out[i] = (uint8_t)(lo == hi ? lo : 0xFFu);
+}
+
 __global__ void k_e4m3(const float *s, int64_t n, uint8_t *out) {
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i < n) out[i] = (uint8_t)e4m3_rn(s[i]);
@@ -119,6 +142,14 @@ int probe_cand_err(const float *y, const uint2 *codes, const float *d, int64_t n
 }
 int probe_e2m1(const float *q, int64_t n, uint8_t *out) {
     k_e2m1<<<(unsigned)((n + 255) / 256), 256>>>(q, n, out);
+    return cudaDeviceSynchronize();
+}
+int probe_sr_f16(const float *q, const uint8_t *r, int64_t n, uint8_t *out) {
+    k_sr_f16<<<(unsigned)((n + 255) / 256), 256>>>(q, r, n, out);
+    return cudaDeviceSynchronize();
+}
+int probe_e2m1_f16(uint8_t *out) {
+    k_e2m1_f16<<<256, 256>>>(out);
     return cudaDeviceSynchronize();
 }
 int probe_e2m1_order(uint32_t *out) {

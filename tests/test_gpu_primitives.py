@@ -37,6 +37,8 @@ def probes(tmp_path_factory):
     lib.probe_e2m1.argtypes = [vp, i64, vp]
     lib.probe_e2m1_order.argtypes = [vp]
     lib.probe_sr.argtypes = [vp, vp, i64, vp]
+    lib.probe_sr_f16.argtypes = [vp, vp, i64, vp]
+    lib.probe_e2m1_f16.argtypes = [vp]
     lib.probe_e4m3.argtypes = [vp, i64, vp]
     lib.probe_e4m3_value.argtypes = [vp]
     lib.probe_e2m1_value.argtypes = [vp]
@@ -103,6 +105,36 @@ def test_sr_round_matches_oracle(probes):
     ref = oracle.e2m1_sr_array(q, r)
     bad = np.nonzero(got != ref)[0]
     assert bad.size == 0, [(float(q[i]), int(r[i]), int(got[i]), int(ref[i])) for i in bad[:8]]
+
+
+def test_sr_f16_pair_matches_oracle(probes):
+    # the fast path's stochastic rounding: quotients at 2^-14 scale, truncated
+    # to f16 pairs, dithered per 16-bit lane, cast from f16x2
+    rng = np.random.default_rng(13)
+    q = np.concatenate([dense_floats(-30, 3, 10, 14), SPECIALS[np.isfinite(SPECIALS)]])
+    q = q[np.abs(q) < 16.0]
+    q = np.repeat(q, 4)
+    r = rng.integers(0, 256, q.size, dtype=np.uint8)
+    qt, rt = torch.from_numpy(q).cuda(), torch.from_numpy(r).cuda()
+    out = torch.empty(q.size, dtype=torch.uint8, device="cuda")
+    assert probes.probe_sr_f16(ptr(qt), ptr(rt), q.size, ptr(out)) == 0
+    got = out.cpu().numpy()
+    ref = oracle.e2m1_sr_array(q, r)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(q[i]), int(r[i]), int(got[i]), int(ref[i])) for i in bad[:8]]
+
+
+def test_e2m1_f16_cast_matches_oracle(probes):
+    # every f16 pattern (the fast path never feeds it NaN), in both halves of the pair
+    out = torch.empty(65536, dtype=torch.uint8, device="cuda")
+    assert probes.probe_e2m1_f16(ptr(out)) == 0
+    got = out.cpu().numpy()
+    with np.errstate(invalid="ignore"):  # NaN patterns widen to NaN
+        vals = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float32)
+    keep = ~np.isnan(vals)
+    ref = oracle.e2m1_rne_array(vals)
+    bad = np.nonzero((got != ref) & keep)[0]
+    assert bad.size == 0, [(float(vals[i]), int(got[i]), int(ref[i])) for i in bad[:8]]
 
 
 def test_e4m3_cast_matches_oracle(probes):
