@@ -59,6 +59,32 @@ __device__ __forceinline__ void strip_block(const uint2 (&w)[16], int cc, f2 (&v
     }
 }
 
+// The same block with the butterfly's first stage applied, (a, b) ->
+// (a + b, a - b) on rows 2m, 2m + 1: for bf16 the even row's element enters
+// the adds as a bf16 operand of a mixed-precision add (it widens exactly, so
+// the result is the fp32 sum), which saves unpacking it.
+template <typename T>
+__device__ __forceinline__ void strip_fwht_first(const uint2 (&w)[16], int cc, f2 (&v)[8]) {
+    if (sizeof(T) != 2) {
+        strip_block<T>(w, cc, v);
+        fwht16_first(v);
+        return;
+    }
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+        const uint32_t a = (cc < 2) ? w[2 * m].x : w[2 * m].y, b = (cc < 2) ? w[2 * m + 1].x : w[2 * m + 1].y;
+        const float fb = (cc & 1) ? bf16_hi(b) : bf16_lo(b);
+        if (cc & 1)
+            asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, hi, %3; sub.rn.f32.bf16 %1, hi, %3; }"
+                : "=f"(v[m].x), "=f"(v[m].y)
+                : "r"(a), "f"(fb));
+        else
+            asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, lo, %3; sub.rn.f32.bf16 %1, lo, %3; }"
+                : "=f"(v[m].x), "=f"(v[m].y)
+                : "r"(a), "f"(fb));
+    }
+}
+
 // Writes a staged output tile of the columnwise layout: output rows
 // o0..o0+TC-1, row blocks rb0..rb0+RBT-1 (codes as 16-byte pieces, scales as
 // words; narrower stores where alignment or the tensor edge requires).  Row
@@ -194,10 +220,14 @@ __global__ void __launch_bounds__(256, 2) k_quant_col(const __grid_constant__ CU
             uint2 c = make_uint2(0u, 0u);
             if (rb < RB && o0 + ol < C) {
                 f2 v[8];
-                strip_block<T>(w, cc, v);
-                if (fast) {
+                if (fast && RHT) {
+                    strip_fwht_first<T>(w, cc, v);
+                    c = encode_block_fast<MODE, RHT, AP, true>(v, sd, tab, signs, rnd[cc], S);
+                } else if (fast) {
+                    strip_block<T>(w, cc, v);
                     c = encode_block_fast<MODE, RHT, AP>(v, sd, tab, signs, rnd[cc], S);
                 } else {
+                    strip_block<T>(w, cc, v);
                     if (RHT) rht16(v, rm);
                     c = encode_block<MODE>(v, sd, tab, rnd[cc], S);
                 }
