@@ -99,6 +99,36 @@ __device__ __forceinline__ uint32_t e2m1x8(float q0, float q1, float q2, float q
     return w;
 }
 
+// Eight fp32 values -> eight codes as e2m1x8, plus each pair's decoded grid
+// values as f16x2 (low half = even element), taken from the cast's own byte
+// before it is packed.
+__device__ __forceinline__ uint32_t e2m1x8_vals(const f2 (&q)[8], int p0, uint32_t (&h)[8]) {
+    uint32_t w;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %8, %7;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %10, %9;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %12, %11;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %4, b3;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(w), "=r"(h[p0]), "=r"(h[p0 + 1]), "=r"(h[p0 + 2]), "=r"(h[p0 + 3])
+        : "f"(q[p0].x), "f"(q[p0].y), "f"(q[p0 + 1].x), "f"(q[p0 + 1].y), "f"(q[p0 + 2].x), "f"(q[p0 + 2].y),
+          "f"(q[p0 + 3].x), "f"(q[p0 + 3].y));
+    return w;
+}
+
+// The two fp32 values of an f16x2 word (low half -> .x).
+__device__ __forceinline__ f2 f16x2_to_f2(uint32_t h2) {
+    f2 v;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }"
+        : "=f"(v.x), "=f"(v.y)
+        : "r"(h2));
+    return v;
+}
+
 // Exact fp32 values of the two codes in byte `b` (low nibble -> .x).
 __device__ __forceinline__ f2 e2m1x2_value(uint32_t b) {
     uint32_t h2;

@@ -130,6 +130,27 @@ __device__ __forceinline__ float candidate_error(const f2 (&y)[8], uint2 codes, 
     return __fadd_rn(p[0].x, p[0].y);
 }
 
+// The same error from the negated candidate values nv = -val (f16x2 pairs,
+// as the fast encoder's cast produces them from the negated quotients):
+// t = RN(nv * (-d)) = RN(val * d), then exactly the steps above.  (Written as
+// t * (+1) + y with t = RN(nv * d), ptxas folds the multiply by one and
+// contracts the product into a single FMA.)
+__device__ __forceinline__ float candidate_error_neg(const f2 (&y)[8], const uint32_t (&nv)[8], float d) {
+    const f2 ndd{-d, -d}, m1{-1.0f, -1.0f}, z{0.0f, 0.0f};
+    f2 p[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const f2 e = fma2(mul2(f16x2_to_f2(nv[k]), ndd), m1, y[k]);
+        p[k] = fma2(e, e, z);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; k++) p[k] = add2(p[k], p[k + 4]);
+    p[0] = add2(p[0], p[2]);
+    p[1] = add2(p[1], p[3]);
+    p[0] = add2(p[0], p[1]);
+    return __fadd_rn(p[0].x, p[0].y);
+}
+
 // Encode one block in the given mode.  Returns the codes and writes S.
 template <int MODE>
 __device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &sd, const DivTable &T,
@@ -205,6 +226,20 @@ __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32
     return c;
 }
 
+// RNE codes of one block (no RHT) plus the negated grid values of every
+// pair for the four-over-six error (the codes are cast from -q and flipped).
+__device__ __forceinline__ uint2 encode_fast_vals(const f2 (&v)[8], const Divisor &D, uint32_t S,
+                                                  uint32_t (&nv)[8]) {
+    f2 nq[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) nq[k] = neg_quot2(v[k], D);
+    const uint32_t keep = S ? 0xFFFFFFFFu : 0u;
+    uint2 c;
+    c.x = (e2m1x8_vals(nq, 0, nv) ^ 0x88888888u) & keep;
+    c.y = (e2m1x8_vals(nq, 4, nv) ^ 0x88888888u) & keep;
+    return c;
+}
+
 // One block on the fast path.  v holds the raw block (RHT: the butterfly is
 // applied here and the 0.25 / signs are folded as above; STAGE1: v already
 // holds the butterfly's first stage).  AP (fast math) replaces the exact
@@ -220,10 +255,11 @@ __device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &s
         const uint32_t S6 = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m6));
         const uint32_t S4 = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m4));
         const Divisor D6 = T.e[S6], D4 = T.e[S4];
-        const uint2 c6 = encode_fast<false>(v, D6, S6, false, signs, rnd);
-        const uint2 c4 = encode_fast<false>(v, D4, S4, false, signs, rnd);
-        const float e6 = candidate_error(v, c6, S6 ? D6.d : 0.0f);
-        const float e4 = candidate_error(v, c4, S4 ? D4.d : 0.0f);
+        uint32_t n6[8], n4[8];  // negated candidate values, straight from the casts
+        const uint2 c6 = encode_fast_vals(v, D6, S6, n6);
+        const uint2 c4 = encode_fast_vals(v, D4, S4, n4);
+        const float e6 = candidate_error_neg(v, n6, S6 ? D6.d : 0.0f);
+        const float e4 = candidate_error_neg(v, n4, S4 ? D4.d : 0.0f);
         const bool pick4 = e4 < e6;  // ties keep map-to-6
         S_out = pick4 ? S4 : S6;
         return pick4 ? c4 : c6;

@@ -126,6 +126,22 @@ __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *ba
 
 // Four-over-six candidate error of block i: values y[16i..], codes packed two
 // per byte (low nibble first) in codes[i], element divisor d[i].
+// The fast path's form: the candidate's values negated (codes with their
+// sign bits flipped), decoded to f16x2 pairs.
+__global__ void k_cand_err_neg(const float *y, const uint2 *codes, const float *d, int64_t n, float *out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    f2 v[8];
+    uint32_t nv[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        v[k] = f2{y[16 * i + 2 * k], y[16 * i + 2 * k + 1]};
+        const uint32_t w = ((k < 4) ? codes[i].x : codes[i].y) ^ 0x88888888u;
+        asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(nv[k]) : "r"((w >> (8 * (k & 3))) & 0xFFu));
+    }
+    out[i] = candidate_error_neg(v, nv, d[i]);
+}
+
 __global__ void k_cand_err(const float *y, const uint2 *codes, const float *d, int64_t n, float *out) {
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -136,6 +152,10 @@ __global__ void k_cand_err(const float *y, const uint2 *codes, const float *d, i
 }
 
 extern "C" {
+int probe_cand_err_neg(const float *y, const uint2 *codes, const float *d, int64_t n, float *out) {
+    k_cand_err_neg<<<(unsigned)((n + 255) / 256), 256>>>(y, codes, d, n, out);
+    return cudaDeviceSynchronize();
+}
 int probe_cand_err(const float *y, const uint2 *codes, const float *d, int64_t n, float *out) {
     k_cand_err<<<(unsigned)((n + 255) / 256), 256>>>(y, codes, d, n, out);
     return cudaDeviceSynchronize();

@@ -44,6 +44,7 @@ def probes(tmp_path_factory):
     lib.probe_e2m1_value.argtypes = [vp]
     lib.probe_div.argtypes = [u64, i64, i32, vp, vp]
     lib.probe_cand_err.argtypes = [vp, vp, vp, i64, vp]
+    lib.probe_cand_err_neg.argtypes = [vp, vp, vp, i64, vp]
     return lib
 
 
@@ -171,11 +172,14 @@ def test_exact_division(probes, kind):
     assert int(bad.item()) == 0, first.cpu().numpy().reshape(-1, 3)[:4]
 
 
-def test_four_over_six_candidate_error_matches_oracle(probes):
+@pytest.mark.parametrize("form", ["codes", "negated_values"])
+def test_four_over_six_candidate_error_matches_oracle(probes, form):
     """Bit-exact squared errors, so that no multiply is fused into the add or
     subtract that follows it (that would change which candidate wins a
     near-tie).  Half of the blocks carry the RNE codes of y/d (errors of a real
-    candidate), half random codes (every code value against every divisor)."""
+    candidate), half random codes (every code value against every divisor).
+    Both forms: from the packed codes, and from the negated f16x2 values the
+    fast encoder takes straight from its casts."""
     n = 1 << 20
     rng = np.random.default_rng(31)
     y = (rng.standard_normal((n, 16)) * np.exp2(rng.integers(-30, 30, (n, 1)))).astype(np.float32)
@@ -193,7 +197,8 @@ def test_four_over_six_candidate_error_matches_oracle(probes):
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
     yt, ct, dt = (torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (y, packed, d))
     out = torch.empty(n, dtype=torch.float32, device="cuda")
-    assert probes.probe_cand_err(ptr(yt), ptr(ct), ptr(dt), n, ptr(out)) == 0
+    fn = probes.probe_cand_err if form == "codes" else probes.probe_cand_err_neg
+    assert fn(ptr(yt), ptr(ct), ptr(dt), n, ptr(out)) == 0
     got = out.cpu().numpy()
     same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
     bad = np.flatnonzero(~same)
