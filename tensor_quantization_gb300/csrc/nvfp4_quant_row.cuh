@@ -4,7 +4,7 @@
 // shared).
 //
 //  k_quant_row               per-tensor global scale (amax from the amax pass
-//                            or given by the caller).  TMA brings 64-row
+//                            or given by the caller).  TMA brings 128-row
 //                            tiles into shared memory; a thread encodes the
 //                            four blocks of one tile row.
 //  k_quant_rowscaled_staged  one global scale per row, rows of up to 96 KiB:
@@ -62,14 +62,14 @@ __device__ __forceinline__ uint2 row_block(const QArgs &a, const ScaleDiv &sd, c
 // ---------------------------------------------------------------------
 // Per-tensor rowwise quantize, input staged through shared memory by TMA.
 //
-// The input is cut into tiles of 64 rows x 64 columns (4 blocks per row).
+// The input is cut into tiles of 128 rows x 64 columns (4 blocks per row).
 // One thread owns one tile row, i.e. 4 consecutive blocks: its codes are 32
 // contiguous bytes and its scales one 32-bit word.  Persistent CTAs walk the
 // tiles round-robin; thread 0 keeps kStages tiles in flight with TMA copies
 // into 128-byte-swizzled buffers, so the 16-byte chunks a warp reads sit in
 // distinct bank groups.  Boxes outside the tensor are zero-filled, which also
 // yields the zero pad bytes of the swizzled scale layout.
-constexpr int kTileRows = 64;
+constexpr int kTileRows = 128;  // 64 measured 0.5 us slower on 8192x4096, 256 1.2 us
 constexpr int kTileCols = 64;
 constexpr int kStages = 1;
 
