@@ -135,7 +135,9 @@ typedef struct {
  * reduction (a running maximum and a few counters).  Allocate
  * nvfp4_workspace_bytes() bytes, 8-byte aligned, and zero them once before
  * first use; every call leaves them zero again.  Calls that share a workspace
- * must not run concurrently on the GPU. */
+ * must not run concurrently on the GPU.  Exception: a call in which a bounded
+ * device-side wait gave up (its global scale comes back NaN although the input
+ * held no NaN) may leave the workspace dirty; zero it before the next call. */
 size_t nvfp4_workspace_bytes(void);
 
 /* Bytes of one scale array for an [rows_out, cols_out] output (swizzle
