@@ -267,6 +267,10 @@ static cudaError_t run_amax_tma(const QArgs &a, cudaStream_t s) {
     if (per_sm < 1) per_sm = 1;
     const int64_t tiles = ((a.rows + kStreamTileRows - 1) / kStreamTileRows) *
                           ((a.cols + kStreamTileCols - 1) / kStreamTileCols);
+    // three CTAs per SM (of four that fit) still keep ~144 KB per SM in flight,
+    // and leave room for the quantize kernel's first CTAs to start on every SM
+    // while the pass drains (-1.3 us per step on 8192x4096; two per SM: no gain)
+    if (per_sm > 3) per_sm = 3;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     k<<<(int)(tiles < cap ? tiles : cap), kAmaxTmaThreads, smem, s>>>(map, a);
     return cudaGetLastError();
