@@ -388,6 +388,33 @@ def test_amax_entry_point():
         assert same_float_bits(a.cpu().numpy(), oa) and same_float_bits(gsc.cpu().numpy(), og)
 
 
+def test_amax_entry_point_dynamic_tiles_and_workspace_reuse():
+    """A tensor large enough that the standalone pass hands out most tiles from
+    its counter (2048 tiles for at most three CTAs per SM): repeated calls,
+    interleaved with quantize calls that share the workspace, give the exact
+    amax every time and leave every workspace word zero."""
+    x = mixed_input(2048, 8192, seed=41)
+    xd = x.cuda()
+    ws = nvfp4.Workspace.get(xd.device)
+    oa, og = oracle.amax(np_bits(x), rht=True)
+    plain = float(x.float().abs().max())
+    for it in range(3):
+        for rht in (True, False):
+            a = torch.empty(1, device="cuda")
+            gsc = torch.empty(1, device="cuda")
+            nvfp4.nvfp4_amax(xd, nvfp4.ROWWISE, rht, 0xFFFF, nvfp4.make_output(amax=a, global_scale=gsc), ws)
+            torch.cuda.synchronize()
+            if rht:
+                assert same_float_bits(a.cpu().numpy(), oa) and same_float_bits(gsc.cpu().numpy(), og)
+            else:
+                assert float(a.item()) == plain
+            assert int(ws.view(torch.int32).abs().sum()) == 0
+        q = nvfp4.quantize(xd, mode="sr", rht=True, sign_mask=0xFFFF, seed=it)
+        torch.cuda.synchronize()
+        assert same_float_bits(q.amax.cpu().numpy(), oa)
+        assert int(ws.view(torch.int32).abs().sum()) == 0
+
+
 # ------------------------------------------------------------ dequantize
 @pytest.mark.parametrize("swizzled", [False, True])
 @pytest.mark.parametrize("per_row", [False, True])
