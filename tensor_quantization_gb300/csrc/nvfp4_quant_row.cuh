@@ -259,9 +259,9 @@ constexpr uint32_t kMaxGridPolls = 1u << 24;  // x >= 64 ns: the grid barrier gi
 // Thread 0 of every CTA: fold the CTA maximum (magnitude bits) into the
 // tensor maximum (ws[0]), count the CTA in (ws[1], ordered after the maximum
 // by release semantics) and wait until every CTA is in; the maximum is final
-// then and is read together with the count in one 64-bit load.  A second
-// count (ws[2]) lets the last CTA out clear ws[0..2] for the next call.
-// Returns false if the wait gave up.
+// then and is read together with the count in one 64-bit load.  Returns false
+// if the wait gave up.  grid_amax_depart (at the end of the kernel, off the
+// critical path) counts the CTA out.
 __device__ __forceinline__ bool grid_amax_barrier(uint32_t *ws, uint32_t m, uint32_t nctas, uint32_t &total) {
     asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(ws), "r"(m) : "memory");
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws + 1) : "memory");
@@ -276,12 +276,18 @@ __device__ __forceinline__ bool grid_amax_barrier(uint32_t *ws, uint32_t m, uint
         if (i >= 4096) __nanosleep(64);  // spin first: the last CTA usually arrives within microseconds
     }
     total = (uint32_t)v;
-    if (atomicAdd(ws + 2, 1u) == nctas - 1) {  // every CTA has read the maximum
+    return ok;
+}
+
+// Thread 0 of every CTA, after its barrier read: a second count (ws[2]) lets
+// the last CTA out, when every CTA has read the maximum, clear ws[0..2] for
+// the next call.
+__device__ __forceinline__ void grid_amax_depart(uint32_t *ws, uint32_t nctas) {
+    if (atomicAdd(ws + 2, 1u) == nctas - 1) {
         ws[0] = 0u;
         ws[1] = 0u;
         ws[2] = 0u;
     }
-    return ok;
 }
 
 template <int MODE, bool RHT, typename T, bool AP>
@@ -438,6 +444,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
         atomicAdd(&g_wait_timeouts, 1u);
         a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
     }
+    if (tid == 0) grid_amax_depart(a.workspace, G);
 }
 
 template <int MODE, bool RHT, typename T>
