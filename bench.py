@@ -66,6 +66,9 @@ def counted_bytes(w: wl.Workload, elem: int = 2) -> dict:
     n = w.rows * w.cols
     codes = sum(r * c // 2 for r, c in orientations(w))
     scales = sum(scale_bytes(r, c, w.swizzled) for r, c in orientations(w))
+    if w.amax_given:  # one read; the given amax is read and g written
+        q = n * elem + codes + scales + 8
+        return {"amax_pass": 0, "quantize": q, "total": q}
     if w.per_row:
         q = n * elem + codes + scales + 8 * w.rows
         return {"amax_pass": 0, "quantize": q, "total": q}
@@ -193,6 +196,7 @@ def aggregate_gbs(bytes_per_rank_step: int, ms_per_step: float, world: int) -> f
 def bench_config(w: wl.Workload, world: int) -> dict:
     """The workload description both arms report."""
     return {"workload": w.name, "rows": w.rows, "cols": w.cols, "input": "bf16", "mode": w.mode, "rht": w.rht,
+            "amax": "given (NVFP4_AMAX_GIVEN, computed before the timed region)" if w.amax_given else "computed",
             "scales": "swizzled_32x4x4" if w.swizzled else "linear",
             "l2": "flushed before every timed step: 512 MiB write + 256 MiB read",
             "parallelism": f"replicas{world}" if world > 1 else "single_gpu"}
@@ -225,6 +229,11 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         scrub.max()  # write-back of the dirty flush lines happens here, untimed
     amax_kernel, quant_kernel = kernel_plan(w)
     split = amax_kernel is not None  # two kernels: amax pass then encode, also timed separately
+    orient_flag = nvfp4.COLWISE if (w.colwise and not w.rowwise) else nvfp4.ROWWISE
+    if w.amax_given:  # the amax a caller would bring (e.g. from delayed scaling), outside the timed region
+        nvfp4.nvfp4_amax(x, orient_flag, w.rht, mask, out, ws, stream)
+        torch.cuda.synchronize(dev)
+        flags |= nvfp4.AMAX_GIVEN
 
     def quant_call(fl):
         if w.mode == "sr" and w.rht:
@@ -235,8 +244,6 @@ def run_ours(args, rank: int, world: int) -> dict | None:
             nvfp4.nvfp4_quantize_four_over_six(x, fl, out, ws, stream)
         else:
             nvfp4.nvfp4_quantize_rne(x, fl, out, ws, stream)
-
-    orient_flag = nvfp4.COLWISE if (w.colwise and not w.rowwise) else nvfp4.ROWWISE
 
     def step(ev0, ev1, ev2):
         ev0.record(stream)
@@ -325,6 +332,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     else:
         dom, dom_bytes, dom_ms = quant_kernel, nbytes["total"], k2
         unit_desc = ("2 B read + 0.5 B codes + 1/16 B scale per element + 8 B of scale words per row" if w.per_row
+                     else "2 B read + 0.5 B codes + 1/16 B scale per element (amax given)" if w.amax_given
                      else "2 B read twice (amax pass, encode) + 0.5 B codes + 1/16 B scale per element")
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = profile_traffic(dom, w.name)
@@ -390,6 +398,8 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
     if w.per_row:
         return None, ("k_quant_rowscaled_staged" if w.cols * 2 <= ROWSCALED_STAGED_MAX_ROW_BYTES
                       else "k_quant_rowscaled")
+    if w.amax_given:  # the quantize kernel alone (the one-kernel path needs to compute the amax)
+        return None, ("k_quant_2d" if w.block2d else "k_quant_col" if not w.rowwise else "k_quant_row")
     if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
         return None, "k_quant_row_fused"
     amax = "k_amax_rht_col" if (w.rht and w.colwise and not w.rowwise) else "k_amax_tma"
@@ -410,24 +420,38 @@ def pad_launch_needed(w: wl.Workload) -> bool:
 
 
 # ------------------------------------------------------------ the oracle
-def oracle_sample(w: wl.Workload, x_cpu: torch.Tensor, mask: int, rows: int):
-    """One oracle pass (amax + encode) over the first `rows` rows."""
+def oracle_sample(w: wl.Workload, x_cpu: torch.Tensor, mask: int, rows: int, amax: float | None = None):
+    """One oracle pass (amax + encode; the encode alone with a given amax)
+    over the first `rows` rows."""
     import numpy as np
 
     import oracle
     xs = x_cpu[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
     for colwise in ([False] if w.rowwise else []) + ([True] if w.colwise else []):
         oracle.quantize(xs, colwise=colwise, mode=w.mode, block2d=w.block2d, per_row=w.per_row,
-                        swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset)
+                        swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset,
+                        amax_given=amax)
+
+
+def given_amax(w: wl.Workload, x_cpu: torch.Tensor, mask: int) -> float | None:
+    """The amax a given-amax workload's calls receive (the oracle's), else None."""
+    if not w.amax_given:
+        return None
+    import numpy as np
+
+    import oracle
+    xs = x_cpu.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return float(oracle.amax(xs, colwise=w.colwise and not w.rowwise, rht=w.rht, sign_mask=mask)[0][0])
 
 
 def cpu_baseline(w: wl.Workload, x_cpu: torch.Tensor, mask: int, min_seconds: float) -> dict:
     import oracle
     oracle.build()
+    A = given_amax(w, x_cpu, mask)
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle_sample(w, x_cpu, mask, w.rows)
+        oracle_sample(w, x_cpu, mask, w.rows, A)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds:
@@ -445,12 +469,13 @@ def run_reference(args) -> dict:
     x_cpu, mask = wl.make_input(w)
     rows = 1024 if w.rows >= 1024 else w.rows
     sub = wl.Workload(**{**w.__dict__, "rows": rows})
+    A = given_amax(w, x_cpu, mask)
     for _ in range(args.warmup):
-        oracle_sample(w, x_cpu, mask, rows)
+        oracle_sample(w, x_cpu, mask, rows, A)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_sample(w, x_cpu, mask, rows)
+        oracle_sample(w, x_cpu, mask, rows, A)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     v = counted_bytes(sub)["total"] / (ms * 1e-3) / 1e9

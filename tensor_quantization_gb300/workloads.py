@@ -17,6 +17,12 @@ The five workloads follow the training recipe's operands:
   along M (columnwise), swizzled scales.
 * ``rowscaled_4o6_8192x8192`` -- rows with log-uniform std in [1e-3, 10],
   per-row global scales, four-over-six, rowwise.
+
+One more measures the single-pass form with a caller-provided amax
+(``NVFP4_AMAX_GIVEN``, e.g. from delayed scaling):
+
+* ``act_rht_sr_given_8192x4096`` -- the activation workload above, quantized
+  with its amax given, so the call is the encode pass alone.
 """
 from __future__ import annotations
 
@@ -42,6 +48,7 @@ class Workload:
     philox_seed: int = 0
     philox_offset: int = 0
     recipe: str = "randn"  # randn | outlier_cols | weight | student_t | rowscaled
+    amax_given: bool = False  # the call gets the per-tensor amax (NVFP4_AMAX_GIVEN): no amax pass
 
     def resized(self, rows: int, cols: int) -> "Workload":
         return replace(self, rows=rows, cols=cols, name=f"{self.name}@{rows}x{cols}")
@@ -62,6 +69,8 @@ WORKLOADS = {
         Workload("grad_col_rht_sr_16384x8192", 16384, 8192, 3, "sr", rht=True, swizzled=True,
                  rowwise=False, colwise=True, philox_seed=3, philox_offset=0, recipe="student_t"),
         Workload("rowscaled_4o6_8192x8192", 8192, 8192, 4, "4o6", per_row=True, recipe="rowscaled"),
+        Workload("act_rht_sr_given_8192x4096", 8192, 4096, 1, "sr", rht=True, swizzled=True,
+                 philox_seed=1, philox_offset=0, recipe="outlier_cols", amax_given=True),
     ]
 }
 

@@ -123,6 +123,7 @@ SMALL = {
     "weight_2d_rne_14336x4096": (272, 512),
     "grad_col_rht_sr_16384x8192": (256, 520),
     "rowscaled_4o6_8192x8192": (96, 1024),
+    "act_rht_sr_given_8192x4096": (520, 1024),
 }
 
 
@@ -131,12 +132,22 @@ def workload_kwargs(w: wl.Workload, mask: int) -> dict:
                 swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset)
 
 
+def workload_runs(w: wl.Workload, x: torch.Tensor, mask: int) -> tuple[dict, dict]:
+    """(GPU call kwargs, oracle kwargs); a given-amax workload passes the
+    oracle's amax to both, so the GPU call runs the encode pass alone."""
+    kw = workload_kwargs(w, mask)
+    if not w.amax_given:
+        return kw, kw
+    a, _ = oracle.amax(np_bits(x), colwise=w.colwise and not w.rowwise, rht=w.rht, sign_mask=mask)
+    return dict(kw, amax=torch.from_numpy(a)), dict(kw, amax=a)
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 def test_workload_small(name):
     w = wl.WORKLOADS[name].resized(*SMALL[name])
     x, mask = wl.make_input(w)
-    kw = workload_kwargs(w, mask)
-    assert_parity(gpu_run(x, **kw), oracle_run(x, **kw))
+    gkw, okw = workload_runs(w, x, mask)
+    assert_parity(gpu_run(x, **gkw), oracle_run(x, **okw))
 
 
 def bands(n: int) -> list[tuple[int, int]]:
@@ -152,8 +163,8 @@ def test_workload_full_size(name):
     plus, for swizzled layouts, every scale byte."""
     w = wl.WORKLOADS[name]
     x, mask = wl.make_input(w)
-    kw = workload_kwargs(w, mask)
-    g = gpu_run(x, **kw)
+    gkw, kw = workload_runs(w, x, mask)
+    g = gpu_run(x, **gkw)
     if w.numel <= 8192 * 4096:
         assert_parity(g, oracle_run(x, **kw))
         return
