@@ -18,11 +18,13 @@ The five workloads follow the training recipe's operands:
 * ``rowscaled_4o6_8192x8192`` -- rows with log-uniform std in [1e-3, 10],
   per-row global scales, four-over-six, rowwise.
 
-One more measures the single-pass form with a caller-provided amax
-(``NVFP4_AMAX_GIVEN``, e.g. from delayed scaling):
+Two more measure follow-up forms on the activation input:
 
-* ``act_rht_sr_given_8192x4096`` -- the activation workload above, quantized
-  with its amax given, so the call is the encode pass alone.
+* ``act_rht_sr_given_8192x4096`` -- quantized with its amax given
+  (``NVFP4_AMAX_GIVEN``, e.g. from delayed scaling), so the call is the encode
+  pass alone.
+* ``act_rht_sr_rowcol_8192x4096`` -- RHT + SR in both orientations (the wgrad
+  operand: rowwise and columnwise codes, one amax and global scale each).
 """
 from __future__ import annotations
 
@@ -71,6 +73,8 @@ WORKLOADS = {
         Workload("rowscaled_4o6_8192x8192", 8192, 8192, 4, "4o6", per_row=True, recipe="rowscaled"),
         Workload("act_rht_sr_given_8192x4096", 8192, 4096, 1, "sr", rht=True, swizzled=True,
                  philox_seed=1, philox_offset=0, recipe="outlier_cols", amax_given=True),
+        Workload("act_rht_sr_rowcol_8192x4096", 8192, 4096, 1, "sr", rht=True, swizzled=True, colwise=True,
+                 philox_seed=1, philox_offset=0, recipe="outlier_cols"),
     ]
 }
 

@@ -124,6 +124,7 @@ SMALL = {
     "grad_col_rht_sr_16384x8192": (256, 520),
     "rowscaled_4o6_8192x8192": (96, 1024),
     "act_rht_sr_given_8192x4096": (520, 1024),
+    "act_rht_sr_rowcol_8192x4096": (528, 1040),
 }
 
 
