@@ -74,6 +74,10 @@ def counted_bytes(w: wl.Workload, elem: int = 2) -> dict:
     if w.amax_given:  # one read; the given amax is read and g written
         q = n * elem + codes + scales + 8
         return {"amax_pass": 0, "quantize": q, "total": q}
+    if w.groups:  # amax pass and encode each read the input once; amax and g per group
+        ng = len(w.groups) - 1
+        a, q = n * elem + 8 * ng, n * elem + codes + scales
+        return {"amax_pass": a, "quantize": q, "total": a + q}
     if two_scales(w):  # one amax read can serve both orientations: counted once, with two amax/g pairs
         a, q = n * elem + 16, n * elem + codes + scales
         return {"amax_pass": a, "quantize": q, "total": a + q}
@@ -226,6 +230,11 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         (nvfp4.SWIZZLED if w.swizzled else 0) | (nvfp4.BLOCK_2D if w.block2d else 0) | \
         (nvfp4.SCALE_PER_ROW if w.per_row else 0)
     q = nvfp4.alloc_outputs(x, flags, w.rht)  # two amax / global scale slots for RHT in both orientations
+    if w.groups:  # one amax / global scale per group
+        offs_d = torch.tensor(w.groups, dtype=torch.int64, device=dev)
+        q = nvfp4.Quantized(q.codes_row, q.scales_row, None, None,
+                            torch.empty(len(w.groups) - 1, dtype=torch.float32, device=dev),
+                            torch.empty(len(w.groups) - 1, dtype=torch.float32, device=dev), flags)
     out = nvfp4.make_output(q.codes_row, q.scales_row, q.codes_col, q.scales_col, q.amax, q.global_scale)
     ws = nvfp4.Workspace.get(dev)
     stream = torch.cuda.current_stream(dev)
@@ -238,7 +247,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     amax_kernel, quant_kernel = kernel_plan(w)
     # two kernels: amax pass then encode, also timed separately (a two-scale
     # call runs four kernels and is timed as one call)
-    split = amax_kernel is not None and not two_scales(w)
+    split = amax_kernel is not None and not multi_kernel_call(w)
     orient_flag = nvfp4.COLWISE if (w.colwise and not w.rowwise) else nvfp4.ROWWISE
     if w.amax_given:  # the amax a caller would bring (e.g. from delayed scaling), outside the timed region
         nvfp4.nvfp4_amax(x, orient_flag, w.rht, mask, out, ws, stream)
@@ -246,7 +255,12 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         flags |= nvfp4.AMAX_GIVEN
 
     def quant_call(fl):
-        if w.mode == "sr" and w.rht:
+        if w.groups:
+            mode = {"rne": nvfp4.MODE_RNE, "4o6": nvfp4.MODE_FOUR_OVER_SIX}.get(
+                w.mode, nvfp4.MODE_RHT_SR if w.rht else nvfp4.MODE_SR)
+            nvfp4.nvfp4_quantize_grouped(x, fl, offs_d, len(w.groups) - 1, mode, mask, w.philox_seed,
+                                         w.philox_offset, out, stream)
+        elif w.mode == "sr" and w.rht:
             nvfp4.nvfp4_quantize_rht_sr(x, fl, mask, w.philox_seed, w.philox_offset, out, ws, stream)
         elif w.mode == "sr":
             nvfp4.nvfp4_quantize_sr(x, fl, w.philox_seed, w.philox_offset, out, ws, stream)
@@ -342,6 +356,9 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     elif two_scales(w):
         dom, dom_bytes, dom_ms = "call", nbytes["total"], k2
         unit_desc = "2 B read twice (amax, encode) + 2 x (0.5 B codes + 1/16 B scale) per element"
+    elif w.groups:
+        dom, dom_bytes, dom_ms = "call", nbytes["total"], k2
+        unit_desc = "2 B read twice (group amaxes, encode) + 0.5 B codes + 1/16 B scale per element"
     else:
         dom, dom_bytes, dom_ms = quant_kernel, nbytes["total"], k2
         unit_desc = ("2 B read + 0.5 B codes + 1/16 B scale per element + 8 B of scale words per row" if w.per_row
@@ -381,8 +398,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         "roofline": roofline,
         "kernels_ms": ({amax_kernel: round(k1, 5), quant_kernel: round(k2, 5), "split_step": round(split_ms, 5),
                         "source": "second loop, event between the passes"} if split else
-                       {"call": round(k2, 5), "source": "the timed steps (four kernels per call)"}
-                       if two_scales(w) else
+                       {"call": round(k2, 5), "source": f"the timed steps ({len(call_kernels(w))} kernels per call)"}
+                       if multi_kernel_call(w) else
                        {quant_kernel: round(k2, 5), "source": "the timed steps (one kernel per call)"}),
         "e2e": {"value": round(nbytes["total"] / (statistics.mean(e2e_ms) * 1e-3) / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -413,6 +430,8 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
     if w.per_row:
         return None, ("k_quant_rowscaled_staged" if w.cols * 2 <= ROWSCALED_STAGED_MAX_ROW_BYTES
                       else "k_quant_rowscaled")
+    if w.groups:
+        return "k_amax_groups", "k_quant_rowscaled_staged"
     if w.amax_given:  # the quantize kernel alone (the one-kernel path needs to compute the amax)
         return None, ("k_quant_2d" if w.block2d else "k_quant_col" if not w.rowwise else "k_quant_row")
     if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
@@ -429,7 +448,14 @@ def call_kernels(w: wl.Workload) -> list[str]:
     """Every kernel one call of this workload launches (the scale pad aside)."""
     if two_scales(w):
         return ["k_amax_tma", "k_quant_row", "k_amax_rht_col", "k_quant_col"]
+    if w.groups:
+        return ["k_amax_groups", "k_group_finalize", "k_quant_rowscaled_staged"]
     return [k for k in kernel_plan(w) if k]
+
+
+def multi_kernel_call(w: wl.Workload) -> bool:
+    """Calls that launch more than an amax pass and one encode: timed as one call."""
+    return two_scales(w) or bool(w.groups)
 
 
 def pad_launch_needed(w: wl.Workload) -> bool:
@@ -449,6 +475,15 @@ def oracle_sample(w: wl.Workload, x_cpu: torch.Tensor, mask: int, rows: int, ama
 
     import oracle
     xs = x_cpu[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    if w.groups:  # each group (clipped to the sample) is its own tensor: amax, then encode
+        for o0, o1 in zip(w.groups[:-1], w.groups[1:]):
+            o1 = min(o1, rows)
+            if o0 >= o1:
+                continue
+            A, _ = oracle.amax(xs[o0:o1], rht=w.rht, sign_mask=mask)
+            oracle.quantize(xs, mode=w.mode, swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed,
+                            offset=w.philox_offset, row_range=(o0, o1), amax_given=float(A[0]))
+        return
     for colwise in ([False] if w.rowwise else []) + ([True] if w.colwise else []):
         oracle.quantize(xs, colwise=colwise, mode=w.mode, block2d=w.block2d, per_row=w.per_row,
                         swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset,

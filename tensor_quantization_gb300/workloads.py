@@ -25,6 +25,9 @@ Two more measure follow-up forms on the activation input:
   pass alone.
 * ``act_rht_sr_rowcol_8192x4096`` -- RHT + SR in both orientations (the wgrad
   operand: rowwise and columnwise codes, one amax and global scale each).
+* ``act_rht_sr_groups_8192x4096`` -- RHT + SR over 8 row groups of uneven
+  sizes (one empty, one of a single row), each with its own amax and global
+  scale (grouped MoE-style quantize).
 """
 from __future__ import annotations
 
@@ -51,6 +54,7 @@ class Workload:
     philox_offset: int = 0
     recipe: str = "randn"  # randn | outlier_cols | weight | student_t | rowscaled
     amax_given: bool = False  # the call gets the per-tensor amax (NVFP4_AMAX_GIVEN): no amax pass
+    groups: tuple = ()  # row offsets of the groups of a grouped call (n_groups + 1), else empty
 
     def resized(self, rows: int, cols: int) -> "Workload":
         return replace(self, rows=rows, cols=cols, name=f"{self.name}@{rows}x{cols}")
@@ -75,6 +79,9 @@ WORKLOADS = {
                  philox_seed=1, philox_offset=0, recipe="outlier_cols", amax_given=True),
         Workload("act_rht_sr_rowcol_8192x4096", 8192, 4096, 1, "sr", rht=True, swizzled=True, colwise=True,
                  philox_seed=1, philox_offset=0, recipe="outlier_cols"),
+        Workload("act_rht_sr_groups_8192x4096", 8192, 4096, 1, "sr", rht=True, swizzled=True,
+                 philox_seed=1, philox_offset=0, recipe="outlier_cols",
+                 groups=(0, 100, 1124, 1124, 4000, 4001, 6000, 7999, 8192)),
     ]
 }
 

@@ -163,6 +163,8 @@ def test_workload_full_size(name):
     rows spread over the tensor (the per-tensor amax always covers all of it)
     plus, for swizzled layouts, every scale byte."""
     w = wl.WORKLOADS[name]
+    if w.groups:
+        pytest.skip("grouped: test_full_size_rht_both_orientations_and_groups covers this input with these group offsets")
     x, mask = wl.make_input(w)
     gkw, kw = workload_runs(w, x, mask)
     g = gpu_run(x, **gkw)
