@@ -85,6 +85,8 @@ __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *ba
     float d, y;
     if (kind == 2) {
         d = __uint_as_float(((mix(a) % 180u) + 47u) << 23 | (b & 0x7FFFFFu));   // 2^-80 .. 2^100
+    } else if (kind == 4) {
+        d = __uint_as_float(((mix(a) % 61u) + 107u) << 23 | (b & 0x7FFFFFu));   // 2^-20 .. 2^40
     } else {
         d = __uint_as_float((127u << 23) | (b & 0x7FFFFFu)) * __uint_as_float(((a >> 27) + 112u) << 23);
     }
@@ -100,6 +102,11 @@ __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *ba
         y = __double2float_rn((double)d * m);
     } else if (kind == 3) {
         y = 0.0f;
+    } else if (kind == 4) {
+        // small quotients, 2^-60 .. 2^-11, with |y| >= 2^-80: the range the
+        // stochastic-rounding fast path uses at its 2^-14 scale; exact there
+        float q = __uint_as_float(((mix(b) % 50u) + 67u) << 23 | (a & 0x7FFFFFu));
+        y = __fmul_rn(d, q);
     } else {
         float q = __uint_as_float((127u << 23) | (a & 0x7FFFFFu)) * __uint_as_float((uint32_t)(112 + (b >> 28)) << 23);
         y = __fmul_rn(d, q);
@@ -111,7 +118,7 @@ __global__ void k_div(uint64_t seed, int64_t n, int kind, unsigned long long *ba
     const float ref = __fdiv_rn(y, d);
     const float want = -(fast ? ref : fminf(fmaxf(ref, -8.f), 8.f));
     bool ok;
-    if (fabsf(ref) < 0x1p-11f && ref != 0.0f) ok = fabsf(nq.x) < 0x1p-10f && signbit(nq.x) != signbit(ref);
+    if (kind != 4 && fabsf(ref) < 0x1p-11f && ref != 0.0f) ok = fabsf(nq.x) < 0x1p-10f && signbit(nq.x) != signbit(ref);
     else ok = __float_as_uint(nq.x) == __float_as_uint(want);
     ok = ok && __float_as_uint(nq.x) == __float_as_uint(nq.y);
     if (fast && fabsf(ref) >= 0x1p-11f && isfinite(ref)) {

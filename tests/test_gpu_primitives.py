@@ -162,7 +162,7 @@ def test_decodes_match_oracle(probes):
         assert np.signbit(got[2 * b]) == bool(b & 8)
 
 
-@pytest.mark.parametrize("kind", [0, 1, 2, 3])
+@pytest.mark.parametrize("kind", [0, 1, 2, 3, 4])
 def test_exact_division(probes, kind):
     bad = torch.zeros(1, dtype=torch.int64, device="cuda")
     first = torch.zeros(12, device="cuda")
