@@ -134,11 +134,39 @@ typedef struct {
 /* Workspace: per-tensor modes need a small device buffer for the amax
  * reduction (a running maximum and a few counters).  Allocate
  * nvfp4_workspace_bytes() bytes, 8-byte aligned, and zero them once before
- * first use; every call leaves them zero again.  Calls that share a workspace
- * must not run concurrently on the GPU.  Exception: a call in which a bounded
- * device-side wait gave up (its global scale comes back NaN although the input
- * held no NaN) may leave the workspace dirty; zero it before the next call. */
+ * first use; every call leaves its counters zero again.  Calls that share a
+ * workspace must not run concurrently on the GPU.
+ *
+ * Failure record: word 3 (bytes 12..15) of the workspace records that a
+ * bounded device-side wait of a call gave up (a TMA copy that never landed, or
+ * the one-kernel path's wait for the other CTAs running past its limit, see
+ * nvfp4_set_wait_limit).  That call's global scale is NaN, and the record is
+ * sticky: every later per-tensor call on the same workspace also publishes a
+ * NaN global scale, until nvfp4_workspace_status reads and clears it.  No
+ * wait blocks forever. */
 size_t nvfp4_workspace_bytes(void);
+
+/* Reads the failure record of a workspace: enqueues a 4-byte device-to-host
+ * copy on `stream` and waits for the stream (the one entry point that
+ * synchronises the host).  Returns NVFP4_ERR_TIMEOUT if a bounded wait of an
+ * earlier call on this workspace gave up, clearing the record (also on the
+ * stream, waited for) so that later calls publish valid scales again;
+ * NVFP4_OK if none did; NVFP4_ERR_INVALID_ARG for a NULL or misaligned
+ * workspace; NVFP4_ERR_CUDA if a copy failed.  The library has no counterpart
+ * on the pages: it is how a caller learns that a device-side wait gave up. */
+nvfp4_status nvfp4_workspace_status(void *workspace, void *stream);
+
+/* Bound of the device-side waits on other CTAs (the grid-wide amax barrier of
+ * the one-kernel path, taken by per-tensor rowwise calls of at most 2^22
+ * elements) in the calls that follow, in polls of the barrier word: a CTA that
+ * sees the barrier still open after `polls` loads gives up, encodes with the
+ * maximum it has seen, and records the failure (see the workspace above).
+ * polls < 0 restores the default of 2^24 polls (about a second: polls after the
+ * first 4096 sleep 64 ns); 0 gives up at once.  Process-wide; returns
+ * NVFP4_ERR_INVALID_ARG above 2^32 - 1.  Waits on TMA copies keep their own
+ * fixed bound.  The pages have no counterpart: this tunes (and lets a test
+ * exercise) the failure path. */
+nvfp4_status nvfp4_set_wait_limit(int64_t polls);
 
 /* Bytes of one scale array for an [rows_out, cols_out] output (swizzle
  * padding included when flags has NVFP4_SWIZZLED). */
@@ -191,8 +219,11 @@ nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16
  * included) apply unchanged.
  *
  * The first call on a device looks the array's device address up
- * (cudaGetSymbolAddress) with that device current and caches it; make that
- * first call before any stream capture.  Every call then clears the scratch
+ * (cudaGetSymbolAddress) with that device current and caches it for the life
+ * of the process; make that first call before any stream capture.  The cached
+ * address does not survive cudaDeviceReset (or any other teardown of the
+ * device's primary context): do not call this entry point after one.  Every
+ * call then clears the scratch
  * on the given stream (it is cleared even when the arguments are rejected; no
  * caller buffer is touched in that case).  All calls share the one array:
  * calls whose work overlaps on the GPU (other streams, other threads) race on

@@ -56,15 +56,29 @@ constexpr int kAmaxTmaThreads = 256;
 // two threads per tile row, two of its four blocks each
 static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "amax thread layout");
 
+//
+// With the RHT, a block is transformed only if it could raise the maximum:
+// every stage of the butterfly rounds |a +- b| to at most RN(|a| + |b|)
+// (rounding is monotone), so no output of a block exceeds 16 max|v|, and a
+// block whose 16 max|v| lies below a maximum some block has already produced
+// cannot change the result.  In a quantize call the CTAs fold their running
+// maximum into the workspace word once per tile and read it back (one tile
+// late), so after the first tiles most blocks cost a bit-max instead of a
+// butterfly; the result is the same maximum, bit for bit.  (The standalone
+// pass, whose last CTA zeroes the word, transforms every block.)
+constexpr bool kAmaxSkip = true;
+
 template <bool RHT, typename T, bool PUBLISH>
 __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_constant__ CUtensorMap tmap,
                                                               const QArgs a) {
     using ST = StreamTile<T>;
+    constexpr bool SKIP = RHT && !PUBLISH && kAmaxSkip;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full[kStreamStages];
     __shared__ __align__(8) uint64_t empty[kStreamStages];
     __shared__ uint32_t stage_tile[kStreamStages];  // tile in the stage, or kNoTile: the stream ended
     __shared__ uint32_t warp_max, warps_in;
+    __shared__ uint32_t cta_run_max, hint_sh;  // SKIP: this CTA's running maximum, the known tensor maximum
     uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
     const uint32_t ntc = (uint32_t)((a.cols + kStreamTileCols - 1) / kStreamTileCols);
     const uint32_t ntiles = ntc * (uint32_t)((a.rows + kStreamTileRows - 1) / kStreamTileRows);
@@ -86,6 +100,8 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
         }
         warp_max = 0u;
         warps_in = 0u;
+        cta_run_max = 0u;
+        hint_sh = 0u;
         mbar_init_fence();
         // dynamic tiles for the standalone pass, whose last CTA publishes (the
         // CTAs then finish together: 1.8 us less on 8192x4096); in a quantize
@@ -103,6 +119,7 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
     __syncthreads();
     bool ok = true;
     uint32_t m = 0;
+    uint32_t hint = 0, sent = 0, pending = 0;  // SKIP state (sent, pending: thread 0's)
     for (uint32_t k = 0;; ++k) {
         const uint32_t s = k % kStreamStages;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (k / kStreamStages) & 1u))) {  // warp-uniform exit
@@ -116,18 +133,41 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
             RawBlock<T> raw;
             stream_block<T>(stage, trow, jb + b, raw);
             if (RHT) {
-                f2 v[8];
-                unpack(raw, v);
-                fwht16(v);
-                m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+                // bits of a value >= 16 max|v| (exactly 16 max|v| for normal
+                // numbers; for subnormals a little more; NaN and Inf stay above
+                // every finite maximum)
+                const uint32_t bound = block_max_bits(raw) + (4u << 23);
+                if (!SKIP || bound > max(m, hint)) {
+                    f2 v[8];
+                    unpack(raw, v);
+                    fwht16(v);
+                    m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+                }
             } else {
                 m = max(m, block_max_bits(raw));
             }
         }
+        if (SKIP) {
+            // warps fold into the CTA word; thread 0 forwards a larger CTA
+            // maximum to the workspace and publishes the tensor maximum it
+            // loaded at the end of the previous tile (no wait on the load)
+            const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
+            if ((tid & 31) == 0 && wm > hint) atomicMax(&cta_run_max, wm);
+            if (tid == 0) {
+                const uint32_t cm = *reinterpret_cast<volatile uint32_t *>(&cta_run_max);
+                if (cm > sent) {
+                    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a.workspace), "r"(cm) : "memory");
+                    sent = cm;
+                }
+                *reinterpret_cast<volatile uint32_t *>(&hint_sh) = max(cm, pending);
+                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(pending) : "l"(a.workspace) : "memory");
+            }
+            hint = max(hint, *reinterpret_cast<volatile uint32_t *>(&hint_sh));
+        }
         ok &= stream_release(empty, k, tid, tid == 0 && !q.done, [&](uint32_t st) { fill(st, q.next()); });
     }
-    if (!ok) {  // a bounded wait gave up: poison the published scale, do not hang
-        atomicAdd(&g_wait_timeouts, 1u);
+    if (!ok) {  // a bounded wait gave up: record it, and a NaN maximum poisons the scale
+        wait_gave_up(a, nullptr);
         m = 0x7FFFFFFFu;
     }
     if (PUBLISH) publish_tensor_amax(a, m, RHT);

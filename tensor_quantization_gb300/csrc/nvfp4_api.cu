@@ -2,6 +2,7 @@
 //
 // Every entry point validates all of its arguments before enqueuing anything,
 // then enqueues kernels on the caller's stream and returns without waiting.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -34,6 +35,10 @@ constexpr int64_t kMaxElems = (int64_t)1 << 34;
 // amax and quantize kernels (the second launched while the first finishes) are
 // as fast or faster (measured on GB300 from 2^19 to 2^27 elements).
 constexpr int64_t kFusedMaxElems = (int64_t)1 << 22;
+
+// Bound of the device-side waits on other CTAs for the calls that follow
+// (nvfp4_set_wait_limit).
+std::atomic<uint32_t> g_grid_polls{nvfp4::kDefaultGridPolls};
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -70,6 +75,7 @@ nvfp4::QArgs make_args(const nvfp4_input *in, const nvfp4_output *out, void *ws,
     a.swizzled = (flags & NVFP4_SWIZZLED) ? 1 : 0;
     a.want_row = (flags & NVFP4_ROWWISE) ? 1 : 0;
     a.want_col = (flags & NVFP4_COLWISE) ? 1 : 0;
+    a.grid_polls = g_grid_polls.load(std::memory_order_relaxed);
     return a;
 }
 
@@ -317,6 +323,26 @@ nvfp4_status nvfp4_dequantize_rht(const uint8_t *codes, const uint8_t *scales, c
                                   int64_t rows, int64_t cols, uint32_t flags, uint16_t sign_mask, void *out,
                                   int32_t out_dtype, void *stream) {
     return dequantize(codes, scales, global_scale, rows, cols, flags, 1, sign_mask, out, out_dtype, stream);
+}
+
+nvfp4_status nvfp4_set_wait_limit(int64_t polls) {
+    if (polls > (int64_t)UINT32_MAX) return NVFP4_ERR_INVALID_ARG;
+    g_grid_polls.store(polls < 0 ? nvfp4::kDefaultGridPolls : (uint32_t)polls, std::memory_order_relaxed);
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_workspace_status(void *workspace, void *stream) {
+    if (!workspace || !aligned(workspace, 8)) return NVFP4_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t *word = static_cast<uint32_t *>(workspace) + 3;  // the give-up record
+    uint32_t rec = 0;
+    if (cudaMemcpyAsync(&rec, word, sizeof(rec), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (rec == 0) return NVFP4_OK;
+    if (cudaMemsetAsync(word, 0, sizeof(rec), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return NVFP4_ERR_TIMEOUT;
 }
 
 const char *nvfp4_status_string(nvfp4_status status) {

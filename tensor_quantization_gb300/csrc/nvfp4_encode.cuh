@@ -43,8 +43,24 @@ struct DivTable {
     Divisor e[128];
 };
 
-__device__ __forceinline__ void build_table(DivTable &T, float g, int tid, int nthreads) {
-    for (int s = tid; s < 128; s += nthreads) T.e[s] = make_divisor(__fmul_rn(e4m3_value((uint32_t)s), g));
+// A divisor times the exact power of two `up` (dn = 1/up): d * up and the
+// reciprocal pieces * dn, each exact while everything stays normal.
+__device__ __forceinline__ Divisor scale_divisor(Divisor D, float up, float dn) {
+    D.d = __fmul_rn(D.d, up);
+    D.nrh = __fmul_rn(D.nrh, dn);
+    D.nrd = __fmul_rn(D.nrd, dn);
+    D.nrl = __fmul_rn(D.nrl, dn);
+    return D;
+}
+
+// The divisor table of g; with up != 1 every entry is pre-multiplied by the
+// fast path's power-of-two factor (FastScale below), so blocks use it as is.
+__device__ __forceinline__ void build_table(DivTable &T, float g, int tid, int nthreads, float up = 1.0f) {
+    for (int s = tid; s < 128; s += nthreads) {
+        Divisor D = make_divisor(__fmul_rn(e4m3_value((uint32_t)s), g));
+        if (up != 1.0f) D = scale_divisor(D, up, 1.0f / up);
+        T.e[s] = D;
+    }
 }
 
 // Divisors M*g of the block-scale computation (M = 6, and 4 for four-over-six).
@@ -190,19 +206,20 @@ __device__ __forceinline__ bool scale_all_fast(float g) {
 // below 2^-40 and keeps its sign, so its code cannot change) and the signs s_j
 // into the code-sign flip.  `signs` holds bit 4e+3 for every negated element
 // e of the 8 in one code word.
-template <bool SR, bool AP = false>
+// The divisor's exact power-of-two factor on the fast path: 4 for the folded
+// RHT, 2^14 for stochastic rounding through fp16 (sr_pair_f16).
+template <int MODE, bool RHT>
+struct FastScale {
+    static constexpr float up = MODE == MODE_SR ? (RHT ? 0x1p16f : 0x1p14f) : (RHT ? 4.0f : 1.0f);
+};
+
+// PRE: D already carries the factor (a table built with FastScale::up).
+template <bool SR, bool AP = false, bool PRE = false>
 __device__ __forceinline__ uint2 encode_fast(const f2 (&v)[8], Divisor D, uint32_t S, bool fold4,
                                              uint2 signs, const uint4 &rnd) {
-    // the divisor's exact power-of-two factor: 4 for the folded RHT, 2^14
-    // for stochastic rounding through fp16 (sr_pair_f16)
     const float up = SR ? (fold4 ? 0x1p16f : 0x1p14f) : (fold4 ? 4.0f : 1.0f);
     const float dn = SR ? (fold4 ? 0x1p-16f : 0x1p-14f) : (fold4 ? 0.25f : 1.0f);
-    if (SR || fold4) {
-        D.d = __fmul_rn(D.d, up);
-        D.nrh = __fmul_rn(D.nrh, dn);
-        D.nrd = __fmul_rn(D.nrd, dn);
-        D.nrl = __fmul_rn(D.nrl, dn);
-    }
+    if ((SR || fold4) && !PRE) D = scale_divisor(D, up, dn);
     f2 nq[8];
     if (AP) {  // fast math: -(y * RN(1/d)), one multiply
 #pragma unroll
@@ -244,7 +261,7 @@ __device__ __forceinline__ uint2 encode_fast_vals(const f2 (&v)[8], const Diviso
 // applied here and the 0.25 / signs are folded as above; STAGE1: v already
 // holds the butterfly's first stage).  AP (fast math) replaces the exact
 // element quotient by y * RN(1/d); block scales stay exact.
-template <int MODE, bool RHT, bool AP = false, bool STAGE1 = false>
+template <int MODE, bool RHT, bool AP = false, bool STAGE1 = false, bool PRE = false>
 __device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &sd, const DivTable &T,
                                                    uint2 signs, const uint4 &rnd, uint32_t &S_out) {
     if (RHT && !STAGE1) fwht16_first(v);
@@ -266,7 +283,7 @@ __device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &s
     } else {
         const uint32_t S = am == 0.0f ? 0u : e4m3_rn(quot_pos(am, sd.m6));
         S_out = S;
-        return encode_fast<MODE == MODE_SR, AP>(v, T.e[S], S, RHT, signs, rnd);
+        return encode_fast<MODE == MODE_SR, AP, PRE>(v, T.e[S], S, RHT, signs, rnd);
     }
 }
 

@@ -37,7 +37,14 @@ struct QArgs {
     // with its own amax / global scale (amax[g] final before the encode)
     const int64_t *group_offsets;
     int64_t n_groups;
+    // bound, in polls, of waits on other CTAs (the one-kernel path's grid
+    // barrier); set by nvfp4_set_wait_limit
+    uint32_t grid_polls;
 };
+
+// Default bound of a wait on other CTAs: 2^24 polls, >= 64 ns each after the
+// first 4096, so about a second.
+constexpr uint32_t kDefaultGridPolls = 1u << 24;
 
 // Device properties, cached per device.
 int sm_count();

@@ -191,8 +191,7 @@ __global__ void __launch_bounds__(16 * kColRBT, 4) k_quant_col(const __grid_cons
         if (t >= ntiles) break;
         const uint32_t s = k & 1u;
         if (!mbar_wait(&full[s], (k >> 1) & 1u)) {
-            atomicAdd(&g_wait_timeouts, 1u);
-            a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
+            wait_gave_up(a, a.gscale);
         }
         const uint32_t tr = t / ntc, tc = t - tr * ntc;
         const uint32_t rb0 = tr * RBT, o0 = tc * TC, rb = rb0 + rbl;
@@ -320,8 +319,7 @@ __global__ void __launch_bounds__(16 * kColRBT, 5) k_quant_2d(const __grid_const
         if (t >= ntiles) break;
         const uint32_t s = k & 1u;
         if (!mbar_wait(&full[s], (k >> 1) & 1u)) {
-            atomicAdd(&g_wait_timeouts, 1u);
-            a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
+            wait_gave_up(a, a.gscale);
         }
         const uint32_t tr = t / ntc, tc = t - tr * ntc;
         const uint32_t rb0 = tr * RBT, o0 = tc * TC, rb = rb0 + rbl, ob = o0 + HC * hc;

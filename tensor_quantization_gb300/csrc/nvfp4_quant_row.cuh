@@ -65,16 +65,18 @@ __device__ __forceinline__ uint2 row_block(const QArgs &a, const ScaleDiv &sd, c
 // The input is cut into tiles of 128 rows x 64 columns (4 blocks per row).
 // One thread owns one tile row, i.e. 4 consecutive blocks: its codes are 32
 // contiguous bytes and its scales one 32-bit word.  Persistent CTAs walk the
-// tiles round-robin; thread 0 keeps kStages tiles in flight with TMA copies
+// tiles round-robin; thread 0 keeps RowTile::kStages tiles in flight with TMA copies
 // into 128-byte-swizzled buffers, so the 16-byte chunks a warp reads sit in
 // distinct bank groups.  Boxes outside the tensor are zero-filled, which also
 // yields the zero pad bytes of the swizzled scale layout.
 constexpr int kTileRows = 128;  // 64 measured 0.5 us slower on 8192x4096, 256 1.2 us
 constexpr int kTileCols = 64;
-constexpr int kStages = 1;
-
 template <typename T>
 struct RowTile {
+    // one stage: the other CTAs of the SM cover a tile's copy (two stages, a
+    // per-warp release of the stage instead of the CTA barrier, and both
+    // together measured the same on 8192x4096)
+    static constexpr int kStages = 1;
     static constexpr int kBoxCols = 128 / (int)sizeof(T);  // one 128-byte swizzle span
     static constexpr int kBoxes = kTileCols / kBoxCols;    // 1 (bf16) or 2 (fp32)
     static constexpr int kBoxBytes = kTileRows * 128;
@@ -108,23 +110,38 @@ __device__ __forceinline__ void issue_tile(const CUtensorMap *map, uint8_t *stag
 
 template <int MODE, bool RHT, typename T, bool AP>
 __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
+    constexpr int kStages = RowTile<T>::kStages;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ DivTable tab;
     __shared__ RhtMult rm;
-    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ __align__(8) uint64_t full[RowTile<T>::kStages];
     uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
     const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, CS = C >> 4, csp = (CS + 3) & ~3u;
     const uint32_t Rp = (R + 127) & ~127u;
     const uint32_t ntc = (C + kTileCols - 1) / kTileCols, ntr = (R + kTileRows - 1) / kTileRows;
     const uint32_t ntiles = ntc * ntr;
     const int tid = threadIdx.x;
+    // tile coordinates advance by the grid size per iteration (no division in
+    // the loop); a second cursor runs kStages tiles ahead for the copies
+    const uint32_t G = gridDim.x, dr = G / ntc, dc = G - dr * ntc;
+    uint32_t tr = blockIdx.x / ntc, tc = blockIdx.x - tr * ntc;
+    uint32_t ir = tr, ic = tc;
+    auto advance = [&](uint32_t &r, uint32_t &c) {
+        c += dc;
+        r += dr;
+        if (c >= ntc) {
+            c -= ntc;
+            ++r;
+        }
+    };
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) mbar_init(&full[s], 1);
         mbar_init_fence();
-        for (int k = 0; k < kStages; k++) {
-            const uint32_t t = blockIdx.x + k * gridDim.x;
-            if (t < ntiles) issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], t / ntc, t % ntc);
-        }
+    }
+    for (int k = 0; k < kStages; k++) {
+        if (tid == 0 && blockIdx.x + k * G < ntiles)
+            issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], ir, ic);
+        advance(ir, ic);
     }
     // per-scale state, built while the first copies are in flight; the amax
     // pass may still be running until grid_dependency_wait returns
@@ -133,9 +150,10 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
     grid_dependency_wait();
     const float A = tensor_amax_read(a, RHT);
     const float g = global_scale_of(A);
-    build_table(tab, g, tid, blockDim.x);
-    const ScaleDiv sd = make_scale_div(g);
     const bool fast = scale_all_fast(g);  // uniform: every divisor in the fast range
+    // on the fast path the table carries the encoder's power-of-two factor
+    build_table(tab, g, tid, blockDim.x, fast ? FastScale<MODE, RHT>::up : 1.0f);
+    const ScaleDiv sd = make_scale_div(g);
     __syncthreads();
     tensor_amax_done(a, A, g);
 
@@ -144,14 +162,12 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
     const bool words = (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
     const bool lin_words = words && (CS & 3u) == 0;
     for (uint32_t k = 0;; ++k) {
-        const uint32_t t = blockIdx.x + k * gridDim.x;
+        const uint32_t t = blockIdx.x + k * G;
         if (t >= ntiles) break;
         const uint32_t s = k % kStages;
         if (!mbar_wait(&full[s], (k / kStages) & 1u)) {  // a copy never landed: bounded, visible failure
-            atomicAdd(&g_wait_timeouts, 1u);
-            a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
+            wait_gave_up(a, a.gscale);
         }
-        const uint32_t tr = t / ntc, tc = t - tr * ntc;
         const uint32_t row = tr * kTileRows + tid, j0 = tc * 4;
         const uint8_t *stage = stages + s * RowTile<T>::kStageBytes;
         if (row < R) {
@@ -170,16 +186,16 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
                                                      (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
                     }
                 }
+                // blocks past the last column arrive zero-filled and encode as
+                // zeros that are not stored: no per-block branch
 #pragma unroll
                 for (int b = 0; b < 4; b++) {
-                    if (j0 + b < CS) {
-                        RawBlock<T> raw;
-                        stage_block<T>(stage, tid, b, raw);
-                        f2 v[8];
-                        if (RHT) unpack_fwht_first(raw, v);
-                        else unpack(raw, v);
-                        c[b] = encode_block_fast<MODE, RHT, AP, true>(v, sd, tab, signs, rnd[b], S[b]);
-                    }
+                    RawBlock<T> raw;
+                    stage_block<T>(stage, tid, b, raw);
+                    f2 v[8];
+                    if (RHT) unpack_fwht_first(raw, v);
+                    else unpack(raw, v);
+                    c[b] = encode_block_fast<MODE, RHT, AP, true, true>(v, sd, tab, signs, rnd[b], S[b]);
                 }
             } else {
 #pragma unroll
@@ -225,14 +241,13 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
                 for (int b = 0; b < 4; b++) dst[b] = 0;
             }
         }
+        advance(tr, tc);
         __syncthreads();  // every thread is done with stage s
-        if (tid == 0) {
-            const uint32_t tn = t + kStages * gridDim.x;
-            if (tn < ntiles) {
-                fence_async_shared();
-                issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], tn / ntc, tn % ntc);
-            }
+        if (tid == 0 && t + kStages * G < ntiles) {
+            fence_async_shared();
+            issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], ir, ic);
         }
+        advance(ir, ic);
     }
 }
 
@@ -254,20 +269,21 @@ constexpr int kFusedTileRows = kStreamTileRows;
 constexpr int kFusedStages = kStreamStages;
 // two threads per tile row, two of its four blocks each
 static_assert(kFusedThreads == 2 * kFusedTileRows && kStreamTileCols == 64, "one-kernel thread layout");
-constexpr uint32_t kMaxGridPolls = 1u << 24;  // x >= 64 ns: the grid barrier gives up after ~1 s
-
 // Thread 0 of every CTA: fold the CTA maximum (magnitude bits) into the
 // tensor maximum (ws[0]), count the CTA in (ws[1], ordered after the maximum
 // by release semantics) and wait until every CTA is in; the maximum is final
-// then and is read together with the count in one 64-bit load.  Returns false
-// if the wait gave up.  grid_amax_depart (at the end of the kernel, off the
-// critical path) counts the CTA out.
-__device__ __forceinline__ bool grid_amax_barrier(uint32_t *ws, uint32_t m, uint32_t nctas, uint32_t &total) {
+// then and is read together with the count in one 64-bit load.  The wait
+// gives up after `polls` loads (QArgs::grid_polls; the default bound is about
+// a second) and returns false.  grid_amax_depart (at the end of the kernel,
+// off the critical path) counts the CTA out either way, so the words return
+// to zero even after a give-up.
+__device__ __forceinline__ bool grid_amax_barrier(uint32_t *ws, uint32_t m, uint32_t nctas, uint32_t polls,
+                                                  uint32_t &total) {
     asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(ws), "r"(m) : "memory");
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws + 1) : "memory");
     bool ok = false;
     unsigned long long v = 0;
-    for (uint32_t i = 0; i < kMaxGridPolls; ++i) {
+    for (uint32_t i = 0; i < polls; ++i) {
         asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ws) : "memory");
         if ((uint32_t)(v >> 32) >= nctas) {
             ok = true;
@@ -353,16 +369,13 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
             mb = __reduce_max_sync(0xFFFFFFFFu, tid < NT / 32 ? red[tid] : 0u);
             if (tid == 0) {
                 uint32_t bits = 0;
-                if (!grid_amax_barrier(a.workspace, mb, G, bits)) {
-                    atomicAdd(&g_wait_timeouts, 1u);
-                    ok = false;
-                }
+                if (!grid_amax_barrier(a.workspace, mb, G, a.grid_polls, bits)) ok = false;
                 float A = __uint_as_float(bits);
                 if (RHT) A = __fmul_rn(A, 0.25f);
                 amax_sh = A;
                 if (blockIdx.x == 0) {
                     a.amax[0] = A;
-                    a.gscale[0] = global_scale_of(A);
+                    publish_gscale(a, a.gscale, global_scale_of(A));
                 }
             }
         }
@@ -440,10 +453,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_quant_row_fused(const __grid_
         }
         ok &= stream_release(empty, L, tid, L + kFusedStages < 2 * nk, [&](uint32_t) { issue(L + kFusedStages); });
     }
-    if (!ok) {  // a bounded wait gave up somewhere in this CTA: the output is not trustworthy
-        atomicAdd(&g_wait_timeouts, 1u);
-        a.gscale[0] = __uint_as_float(0x7FFFFFFFu);
-    }
+    if (!ok) wait_gave_up(a, a.gscale);  // a bounded wait gave up in this CTA: the output is not trustworthy
     if (tid == 0) grid_amax_depart(a.workspace, G);
 }
 
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(256) k_quant_rowscaled_staged(const QArgs a, u
         if (r >= a.rows) break;
         const uint32_t s = k % kRowBufs, par = k & 1u;
         const bool arrived = mbar_wait(&full[s], (k / kRowBufs) & 1u);
-        if (!arrived) atomicAdd(&g_wait_timeouts, 1u);
+        if (!arrived) wait_gave_up(a, nullptr);  // the row's scale is poisoned below
         const uint8_t *rowp = bufs + s * buf_bytes;
         // pass 1: amax of the row (post-RHT magnitudes, 0.25 applied to the max);
         // grouped scaling instead reads the final amax of the row's group

@@ -22,6 +22,33 @@
 
 namespace nvfp4 {
 
+// ------------------------------------------------------- give-up records
+// Workspace word 3 records that a bounded device-side wait gave up.  It is
+// sticky: no kernel clears it, so every later call on the same workspace
+// publishes a NaN global scale until the host reads and clears the word
+// (nvfp4_workspace_status).  A kernel that gives up sets the word, fences,
+// then stores NaN into its global scale; the CTA that publishes the global
+// scale stores it, fences, then re-reads the word and stores NaN if it is
+// set.  With both fences sequentially consistent, either the publisher sees
+// the record or its store precedes the NaN: the NaN always wins.
+constexpr int kStatusWord = 3;
+
+__device__ __forceinline__ void wait_gave_up(const QArgs &a, float *gs) {
+    atomicAdd(&g_wait_timeouts, 1u);
+    if (a.workspace) atomicOr(a.workspace + kStatusWord, 1u);
+    __threadfence();
+    if (gs) *reinterpret_cast<volatile float *>(gs) = __uint_as_float(0x7FFFFFFFu);
+}
+
+__device__ __forceinline__ void publish_gscale(const QArgs &a, float *gs, float g) {
+    *reinterpret_cast<volatile float *>(gs) = g;
+    if (!a.workspace) return;
+    __threadfence();
+    uint32_t st;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(st) : "l"(a.workspace + kStatusWord) : "memory");
+    if (st) *reinterpret_cast<volatile float *>(gs) = __uint_as_float(0x7FFFFFFFu);
+}
+
 // End of an amax pass whose consumer is a quantize kernel: one red.max per CTA.
 __device__ __forceinline__ void fold_tensor_amax(const QArgs &a, uint32_t m) {
     __shared__ uint32_t red[32];
@@ -64,7 +91,7 @@ __device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, 
             float A = __uint_as_float(bits);
             if (rht) A = __fmul_rn(A, 0.25f);
             a.amax[0] = A;
-            a.gscale[0] = global_scale_of(A);
+            publish_gscale(a, a.gscale, global_scale_of(A));
         }
     }
 }
@@ -96,7 +123,7 @@ __device__ __forceinline__ void tensor_amax_done(const QArgs &a, float A, float 
         }
         if (blockIdx.x == 0) a.amax[0] = A;
     }
-    if (blockIdx.x == 0) a.gscale[0] = g;
+    if (blockIdx.x == 0) publish_gscale(a, a.gscale, g);
 }
 
 }  // namespace nvfp4

@@ -46,7 +46,7 @@ class Output(ctypes.Structure):
 EXPORTS = ("nvfp4_workspace_bytes", "nvfp4_scale_bytes", "nvfp4_amax", "nvfp4_quantize_rne",
            "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr", "nvfp4_quantize_four_over_six",
            "nvfp4_dequantize", "nvfp4_status_string", "nvfp4_quantize_rht_sr_static", "nvfp4_quantize_grouped",
-           "nvfp4_dequantize_rht")
+           "nvfp4_dequantize_rht", "nvfp4_workspace_status", "nvfp4_set_wait_limit")
 MODE_RNE, MODE_SR, MODE_RHT_SR, MODE_FOUR_OVER_SIX = 0, 1, 2, 3
 
 
@@ -79,9 +79,12 @@ def load(path: str | None = None):
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, u32, vp, i32, vp]
     L.nvfp4_quantize_grouped.argtypes = [PI, u32, vp, i64, i32, ctypes.c_uint16, u64, u64, PO, vp]
     L.nvfp4_dequantize_rht.argtypes = [vp, vp, vp, i64, i64, u32, ctypes.c_uint16, vp, i32, vp]
+    L.nvfp4_workspace_status.argtypes = [vp, vp]
+    L.nvfp4_set_wait_limit.argtypes = [i64]
     for f in ("nvfp4_amax", "nvfp4_quantize_rne", "nvfp4_quantize_sr", "nvfp4_quantize_rht_sr",
               "nvfp4_quantize_four_over_six", "nvfp4_dequantize", "nvfp4_quantize_rht_sr_static",
-              "nvfp4_quantize_grouped", "nvfp4_dequantize_rht"):
+              "nvfp4_quantize_grouped", "nvfp4_dequantize_rht", "nvfp4_workspace_status",
+              "nvfp4_set_wait_limit"):
         getattr(L, f).restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -145,6 +148,20 @@ def nvfp4_workspace_bytes() -> int:
 
 def nvfp4_scale_bytes(rows_out: int, cols_out: int, flags: int) -> int:
     return int(load().nvfp4_scale_bytes(rows_out, cols_out, flags))
+
+
+def nvfp4_workspace_status(workspace, stream=None) -> int:
+    """The workspace's failure record: OK, or ERR_TIMEOUT (then cleared) if a
+    bounded device-side wait of an earlier call gave up.  Waits for the stream."""
+    st = load().nvfp4_workspace_status(_ptr(workspace), _stream(stream))
+    if st not in (OK, ERR_TIMEOUT):
+        raise NVFP4Error(st, "nvfp4_workspace_status")
+    return st
+
+
+def nvfp4_set_wait_limit(polls: int) -> None:
+    """Bound of the device-side waits on other CTAs for later calls (< 0: default)."""
+    _check(load().nvfp4_set_wait_limit(polls), "nvfp4_set_wait_limit")
 
 
 def nvfp4_amax(x, flags, use_rht, sign_mask, out: Output, workspace, stream=None) -> None:

@@ -106,3 +106,11 @@ def test_arguments_are_rejected_before_any_launch(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(OSError):
         nvfp4.load(str(tmp_path / "missing.so"))
+
+
+def test_failure_record_and_wait_limit_arguments(lib):
+    assert lib.nvfp4_workspace_status(None, None) == nvfp4.ERR_INVALID_ARG
+    assert lib.nvfp4_workspace_status(ctypes.c_void_p(12), None) == nvfp4.ERR_INVALID_ARG  # misaligned
+    assert lib.nvfp4_set_wait_limit(1 << 32) == nvfp4.ERR_INVALID_ARG
+    assert lib.nvfp4_set_wait_limit(0) == nvfp4.OK
+    assert lib.nvfp4_set_wait_limit(-1) == nvfp4.OK  # back to the default

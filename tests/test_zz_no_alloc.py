@@ -2,8 +2,11 @@
 cannot allocate device memory (its amax scratch lives inside the library).
 
 It must give exactly the outputs of nvfp4_quantize_rht_sr with a caller
-workspace, on consecutive calls, through the C ABI.  This file is collected
-last so that a stop at the first failure has already run every other test.
+workspace, and of the CPU oracle, on consecutive calls, through the C ABI:
+on the two-kernel path (amax pass, then quantize) and on the one-kernel path
+of small rowwise tensors (whose grid barrier uses three scratch words).  This
+file is collected last so that a stop at the first failure has already run
+every other test.
 """
 import ctypes
 
@@ -11,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tensor_quantization_gb300 import nvfp4
 from tensor_quantization_gb300 import workloads as wl
 
@@ -42,10 +46,13 @@ def _host(q):
                                                       "amax", "global_scale") if getattr(q, k) is not None}
 
 
-@pytest.mark.parametrize("orient", ["row", "col"])
-def test_static_entry_point_matches_workspace_entry_point(lib, orient):
-    w = wl.WORKLOADS["act_rht_sr_8192x4096"].resized(1024, 2048)
+@pytest.mark.parametrize("orient,rows,cols", [("row", 1024, 2048), ("col", 1024, 2048), ("row", 256, 1024)])
+def test_static_entry_point_matches_workspace_entry_point(lib, orient, rows, cols):
+    w = wl.WORKLOADS["act_rht_sr_8192x4096"].resized(rows, cols)
     x_cpu, mask = wl.make_input(w)
+    xb = x_cpu.view(torch.int16).numpy().view(np.uint16)
+    want = oracle.quantize(xb, colwise=orient == "col", mode="sr", swizzled=True, rht=True, sign_mask=mask,
+                           seed=1, offset=7)
     x = x_cpu.cuda()
     flags = (nvfp4.ROWWISE if orient == "row" else nvfp4.COLWISE) | nvfp4.SWIZZLED
     ref_q, ref_o = _outputs(x, flags)
@@ -63,6 +70,11 @@ def test_static_entry_point_matches_workspace_entry_point(lib, orient):
         got = _host(q)
         for k, v in ref.items():
             assert np.array_equal(got[k].view(np.uint8), v.view(np.uint8)), k
+        codes, scales = (got["codes_row"], got["scales_row"]) if orient == "row" else \
+            (got["codes_col"], got["scales_col"])
+        assert np.array_equal(codes, want["codes"])
+        assert np.array_equal(scales.ravel(), want["scales"].ravel())
+        assert got["global_scale"].view(np.uint32)[0] == want["global_scale"].view(np.uint32)[0]
 
 
 def test_static_entry_point_rejects_bad_sizes(lib):
