@@ -78,7 +78,7 @@ def counted_bytes(w: wl.Workload, elem: int = 2) -> dict:
         ng = len(w.groups) - 1
         a, q = n * elem + 8 * ng, n * elem + codes + scales
         return {"amax_pass": a, "quantize": q, "total": a + q}
-    if two_scales(w):  # one amax read can serve both orientations: counted once, with two amax/g pairs
+    if two_scales(w):  # one amax read serves both orientations, with two amax/g pairs
         a, q = n * elem + 16, n * elem + codes + scales
         return {"amax_pass": a, "quantize": q, "total": a + q}
     if w.per_row:
@@ -436,7 +436,8 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
         return None, ("k_quant_2d" if w.block2d else "k_quant_col" if not w.rowwise else "k_quant_row")
     if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
         return None, "k_quant_row_fused"
-    amax = "k_amax_rht_col" if (w.rht and w.colwise and not w.rowwise) else "k_amax_tma"
+    # bf16 RHT column blocks (alone, or with the row blocks of the same read)
+    amax = "k_amax_tma_cols" if (w.rht and w.colwise) else "k_amax_tma"
     if w.block2d:
         return amax, "k_quant_2d"
     if w.colwise and not w.rowwise:
@@ -446,8 +447,8 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
 
 def call_kernels(w: wl.Workload) -> list[str]:
     """Every kernel one call of this workload launches (the scale pad aside)."""
-    if two_scales(w):
-        return ["k_amax_tma", "k_quant_row", "k_amax_rht_col", "k_quant_col"]
+    if two_scales(w):  # one amax read for both orientations
+        return ["k_amax_tma_cols", "k_quant_row", "k_quant_col"]
     if w.groups:
         return ["k_amax_groups", "k_group_finalize", "k_quant_rowscaled_staged"]
     return [k for k in kernel_plan(w) if k]

@@ -64,21 +64,63 @@ static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "
 // cannot change the result.  In a quantize call the CTAs fold their running
 // maximum into the workspace word once per tile and read it back (one tile
 // late), so after the first tiles most blocks cost a bit-max instead of a
-// butterfly; the result is the same maximum, bit for bit.  (The standalone
-// pass, whose last CTA zeroes the word, transforms every block.)
+// butterfly; the result is the same maximum, bit for bit.  Only thread 0 of a
+// CTA sends to the workspace word, so in the standalone pass its last hint
+// precedes its ticket, and the last ticket's reset comes after every hint.
 constexpr bool kAmaxSkip = true;
+
+// A known lower bound of the tensor maximum for the skip test, shared through
+// one workspace word: each warp folds its running maximum into a CTA word once
+// per tile; thread 0 forwards a larger CTA maximum to the workspace with one
+// red.max and publishes, for the next tile, the workspace value it loaded at
+// the end of the previous tile (so no thread waits on the load).  Every value
+// it ever holds is a maximum some block has produced.
+struct MaxHint {
+    uint32_t *cta_max, *shared_hint;  // shared words, zeroed before the CTA's first barrier
+    uint32_t *word;                   // the workspace word
+    uint32_t hint, sent, pending;     // sent, pending: thread 0's
+
+    __device__ __forceinline__ MaxHint(uint32_t *cm, uint32_t *sh, uint32_t *w)
+        : cta_max(cm), shared_hint(sh), word(w), hint(0u), sent(0u), pending(0u) {}
+
+    // Blocks whose bound is not above this cannot raise the maximum.
+    __device__ __forceinline__ uint32_t threshold(uint32_t m) const { return max(m, hint); }
+
+    __device__ __forceinline__ void fold(uint32_t m) {
+        const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
+        if ((threadIdx.x & 31) == 0 && wm > hint) atomicMax(cta_max, wm);
+        if (threadIdx.x == 0) {
+            const uint32_t cm = *reinterpret_cast<volatile uint32_t *>(cta_max);
+            if (cm > sent) {
+                asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(word), "r"(cm) : "memory");
+                sent = cm;
+            }
+            *reinterpret_cast<volatile uint32_t *>(shared_hint) = max(cm, pending);
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(pending) : "l"(word) : "memory");
+        }
+        hint = max(hint, *reinterpret_cast<volatile uint32_t *>(shared_hint));
+    }
+};
+
+// Bits of a value >= 16 max|v| of a raw 1x16 block: exactly 16 max|v| for
+// normal numbers, a little more for subnormals; NaN and Inf stay above every
+// finite maximum.  No butterfly output of the block exceeds it.
+template <typename T>
+__device__ __forceinline__ uint32_t butterfly_bound(const RawBlock<T> &raw) {
+    return block_max_bits(raw) + (4u << 23);
+}
 
 template <bool RHT, typename T, bool PUBLISH>
 __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_constant__ CUtensorMap tmap,
                                                               const QArgs a) {
     using ST = StreamTile<T>;
-    constexpr bool SKIP = RHT && !PUBLISH && kAmaxSkip;
+    constexpr bool SKIP = RHT && kAmaxSkip;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full[kStreamStages];
     __shared__ __align__(8) uint64_t empty[kStreamStages];
     __shared__ uint32_t stage_tile[kStreamStages];  // tile in the stage, or kNoTile: the stream ended
     __shared__ uint32_t warp_max, warps_in;
-    __shared__ uint32_t cta_run_max, hint_sh;  // SKIP: this CTA's running maximum, the known tensor maximum
+    __shared__ uint32_t cta_run_max, hint_sh;  // SKIP: the MaxHint words
     uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
     const uint32_t ntc = (uint32_t)((a.cols + kStreamTileCols - 1) / kStreamTileCols);
     const uint32_t ntiles = ntc * (uint32_t)((a.rows + kStreamTileRows - 1) / kStreamTileRows);
@@ -119,7 +161,7 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
     __syncthreads();
     bool ok = true;
     uint32_t m = 0;
-    uint32_t hint = 0, sent = 0, pending = 0;  // SKIP state (sent, pending: thread 0's)
+    MaxHint hint(&cta_run_max, &hint_sh, a.workspace);
     for (uint32_t k = 0;; ++k) {
         const uint32_t s = k % kStreamStages;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (k / kStreamStages) & 1u))) {  // warp-uniform exit
@@ -133,11 +175,7 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
             RawBlock<T> raw;
             stream_block<T>(stage, trow, jb + b, raw);
             if (RHT) {
-                // bits of a value >= 16 max|v| (exactly 16 max|v| for normal
-                // numbers; for subnormals a little more; NaN and Inf stay above
-                // every finite maximum)
-                const uint32_t bound = block_max_bits(raw) + (4u << 23);
-                if (!SKIP || bound > max(m, hint)) {
+                if (!SKIP || butterfly_bound(raw) > hint.threshold(m)) {
                     f2 v[8];
                     unpack(raw, v);
                     fwht16(v);
@@ -147,23 +185,7 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
                 m = max(m, block_max_bits(raw));
             }
         }
-        if (SKIP) {
-            // warps fold into the CTA word; thread 0 forwards a larger CTA
-            // maximum to the workspace and publishes the tensor maximum it
-            // loaded at the end of the previous tile (no wait on the load)
-            const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
-            if ((tid & 31) == 0 && wm > hint) atomicMax(&cta_run_max, wm);
-            if (tid == 0) {
-                const uint32_t cm = *reinterpret_cast<volatile uint32_t *>(&cta_run_max);
-                if (cm > sent) {
-                    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a.workspace), "r"(cm) : "memory");
-                    sent = cm;
-                }
-                *reinterpret_cast<volatile uint32_t *>(&hint_sh) = max(cm, pending);
-                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(pending) : "l"(a.workspace) : "memory");
-            }
-            hint = max(hint, *reinterpret_cast<volatile uint32_t *>(&hint_sh));
-        }
+        if (SKIP) hint.fold(m);
         ok &= stream_release(empty, k, tid, tid == 0 && !q.done, [&](uint32_t st) { fill(st, q.next()); });
     }
     if (!ok) {  // a bounded wait gave up: record it, and a NaN maximum poisons the scale
@@ -172,6 +194,125 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
     }
     if (PUBLISH) publish_tensor_amax(a, m, RHT);
     else fold_tensor_amax_warps(a, m, &warp_max, &warps_in);
+}
+
+// RHT blocks along the columns (16 rows of one column), and optionally the
+// row blocks too, from one TMA stream of the bf16 input (the tiles and stages
+// of k_amax_tma).  A warp takes a 16-row strip of the tile and each lane two
+// adjacent columns of it: sixteen 32-bit reads, one per row, that the 32 lanes
+// spread over the row's 128 bytes without bank conflicts.  With ROW, thread t
+// also reduces row blocks 2h, 2h+1 of tile row t % 128 (h = t / 128), as
+// k_amax_tma does, so both orientations' maxima come from one read of the
+// input (the operand of a weight-gradient GEMM needs both).  Both use the
+// skip test above.  The column maximum goes to workspace word kColWord (4)
+// when ROW is set, else to word 0; the row maximum to word 0.  PUBLISH (the
+// standalone pass, columns only): the last CTA publishes amax and g.
+template <bool ROW, bool PUBLISH>
+__global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma_cols(const __grid_constant__ CUtensorMap tmap,
+                                                                   const QArgs a) {
+    static_assert(!(ROW && PUBLISH), "the two-orientation pass hands its maxima to quantize kernels");
+    using T = bf16_t;
+    using ST = StreamTile<T>;
+    constexpr uint32_t kColWord = ROW ? 4u : 0u;
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ __align__(8) uint64_t full[kStreamStages];
+    __shared__ __align__(8) uint64_t empty[kStreamStages];
+    __shared__ uint32_t redr[kAmaxTmaThreads / 32], redc[kAmaxTmaThreads / 32];
+    __shared__ uint32_t hint_words[4];  // MaxHint words: rows (0, 1), columns (2, 3)
+    uint8_t *stages = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
+    const uint32_t ntc = (uint32_t)((a.cols + kStreamTileCols - 1) / kStreamTileCols);
+    const uint32_t ntiles = ntc * (uint32_t)((a.rows + kStreamTileRows - 1) / kStreamTileRows), G = gridDim.x;
+    const uint32_t nk = blockIdx.x < ntiles ? (ntiles - blockIdx.x + G - 1) / G : 0;  // my tiles
+    const int tid = threadIdx.x, trow = tid % kStreamTileRows, jb = (tid / kStreamTileRows) * 2;
+    const int strip = tid >> 5, cbyte = (tid & 31) * 4;  // 16-row strip, byte of the lane's column pair
+    auto issue = [&](uint32_t k) {
+        const uint32_t t = blockIdx.x + k * G, s = k % kStreamStages;
+        stream_issue<T>(&tmap, stages + s * ST::kStageBytes, &full[s], t / ntc, t % ntc);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kStreamStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kAmaxTmaThreads / 32);
+        }
+        for (int i = 0; i < 4; i++) hint_words[i] = 0u;
+        mbar_init_fence();
+        for (uint32_t k = 0; k < nk && k < (uint32_t)kStreamStages; k++) issue(k);
+    }
+    __syncthreads();
+    MaxHint hr(&hint_words[0], &hint_words[1], a.workspace), hc(&hint_words[2], &hint_words[3], a.workspace + kColWord);
+    bool ok = true;
+    uint32_t mr = 0, mc = 0;
+    for (uint32_t k = 0; k < nk; ++k) {
+        const uint32_t s = k % kStreamStages;
+        ok &= mbar_wait(&full[s], (k / kStreamStages) & 1u);
+        const uint8_t *stage = stages + s * ST::kStageBytes;
+        if (ROW) {
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                RawBlock<T> raw;
+                stream_block<T>(stage, trow, jb + b, raw);
+                if (!kAmaxSkip || butterfly_bound(raw) > hr.threshold(mr)) {
+                    f2 v[8];
+                    unpack(raw, v);
+                    fwht16(v);
+                    mr = max(mr, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+                }
+            }
+        }
+        // the strip: word i holds row i of the lane's two columns (low half:
+        // the even column); chunk c of a 128-byte row sits at c ^ (row % 8)
+        uint32_t w[16];
+        uint32_t mx = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int r = strip * 16 + i;
+            w[i] = *reinterpret_cast<const uint32_t *>(stage + r * 128 + ((((cbyte >> 4) ^ (r & 7)) << 4) | (cbyte & 15)));
+            asm("max.u16x2 %0, %1, %2;" : "=r"(mx) : "r"(mx), "r"(w[i] & 0x7FFF7FFFu));
+        }
+        const uint32_t thr = hc.threshold(mc);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const uint32_t bound = (h ? (mx & 0xFFFF0000u) : (mx << 16)) + (4u << 23);
+            if (!kAmaxSkip || bound > thr) {
+                f2 v[8];
+#pragma unroll
+                for (int p = 0; p < 8; p++)
+                    v[p] = h ? f2{bf16_hi(w[2 * p]), bf16_hi(w[2 * p + 1])} : f2{bf16_lo(w[2 * p]), bf16_lo(w[2 * p + 1])};
+                fwht16(v);
+                mc = max(mc, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+            }
+        }
+        if (kAmaxSkip) {
+            if (ROW) hr.fold(mr);
+            hc.fold(mc);
+        }
+        ok &= stream_release(empty, k, tid, k + kStreamStages < nk, [&](uint32_t) { issue(k + kStreamStages); });
+    }
+    if (!ok) {  // a bounded wait gave up: record it, and NaN maxima poison both scales
+        wait_gave_up(a, nullptr);
+        mr = mc = 0x7FFFFFFFu;
+    }
+    if (PUBLISH) {
+        publish_tensor_amax(a, mc, true);
+        return;
+    }
+    allow_dependents();  // the quantize kernel may start staging its tiles
+    mr = __reduce_max_sync(0xFFFFFFFFu, mr);
+    mc = __reduce_max_sync(0xFFFFFFFFu, mc);
+    if ((tid & 31) == 0) {
+        redr[tid >> 5] = mr;
+        redc[tid >> 5] = mc;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        mr = __reduce_max_sync(0xFFFFFFFFu, tid < kAmaxTmaThreads / 32 ? redr[tid] : 0u);
+        mc = __reduce_max_sync(0xFFFFFFFFu, tid < kAmaxTmaThreads / 32 ? redc[tid] : 0u);
+        if (tid == 0) {
+            if (ROW) asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a.workspace), "r"(mr) : "memory");
+            asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a.workspace + kColWord), "r"(mc)
+                         : "memory");
+        }
+    }
 }
 
 // RHT blocks along columns: a thread owns 16 rows x one 16-byte chunk.
@@ -316,10 +457,39 @@ static cudaError_t run_amax_tma(const QArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <bool ROW, bool PUBLISH>
+static cudaError_t run_amax_tma_cols(const QArgs &a, cudaStream_t s) {
+    auto k = k_amax_tma_cols<ROW, PUBLISH>;
+    constexpr int smem = StreamTile<bf16_t>::kSmemBytes;
+    static bool configured = false;  // one attribute call per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    CUtensorMap map;
+    if (!make_tmap_2d(&map, a.x, 2, a.rows, a.cols, a.ld, StreamTile<bf16_t>::kBoxCols, kStreamTileRows))
+        return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAmaxTmaThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 3) per_sm = 3;  // as k_amax_tma: room for the quantize kernel's first CTAs
+    const int64_t tiles = ((a.rows + kStreamTileRows - 1) / kStreamTileRows) *
+                          ((a.cols + kStreamTileCols - 1) / kStreamTileCols);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    k<<<(int)(tiles < cap ? tiles : cap), kAmaxTmaThreads, smem, s>>>(map, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax_cols(const QArgs &a, bool with_rows, cudaStream_t s) {
+    return with_rows ? run_amax_tma_cols<true, false>(a, s) : run_amax_tma_cols<false, false>(a, s);
+}
+
 template <typename T, bool PUBLISH>
 static cudaError_t run_amax_tensor(const QArgs &a, bool rht, bool col, cudaStream_t s) {
     constexpr int W = Chunk<T>::W;
     if (!col) return rht ? run_amax_tma<true, T, PUBLISH>(a, s) : run_amax_tma<false, T, PUBLISH>(a, s);
+    if (PUBLISH && sizeof(T) == 2) return run_amax_tma_cols<false, true>(a, s);
     auto k = k_amax_rht_col<T, PUBLISH>;
     k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
     return cudaGetLastError();

@@ -144,10 +144,14 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
     } else if (per_row) {
         st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, mode, rht, s));
     } else {
-        if (!given) {  // (both orientations with the RHT: the rowwise amax first)
+        // bf16 RHT column blocks: one TMA pass, which with both orientations
+        // also reduces the row blocks (two maxima from one read)
+        const bool tma_cols = rht && want_col && !fp32 && !block2d;
+        if (!given) {
             // the next quantize kernel takes the amax from the workspace and
             // publishes it; a second one reads the published amax[0]
-            st = cuda_status(nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col && !want_row, false, s));
+            st = cuda_status(tma_cols ? nvfp4::launch_amax_cols(a, want_row, s)
+                                      : nvfp4::launch_amax_tensor(a, fp32, rht, rht && want_col && !want_row, false, s));
             if (st != NVFP4_OK) return st;
             a.amax_in_ws = 1;
         }
@@ -162,7 +166,8 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
             ac.gscale = out->global_scale + 1;
             ac.blk_base = base_col;
             st = cuda_status(nvfp4::launch_quant_row(ar, fp32, mode, rht, s));
-            if (st == NVFP4_OK && !given) st = cuda_status(nvfp4::launch_amax_tensor(ac, fp32, rht, true, false, s));
+            if (tma_cols) ac.amax_word = 4;  // the column maximum of the one read
+            else if (st == NVFP4_OK && !given) st = cuda_status(nvfp4::launch_amax_tensor(ac, fp32, rht, true, false, s));
             if (st == NVFP4_OK) st = cuda_status(nvfp4::launch_quant_col(ac, fp32, mode, rht, s));
         } else {
             if (want_row) {

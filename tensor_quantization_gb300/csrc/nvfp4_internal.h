@@ -33,6 +33,9 @@ struct QArgs {
     // the per-tensor amax comes from this call's amax pass through the
     // workspace (the quantize kernel publishes it) instead of amax[0]
     int amax_in_ws;
+    // workspace word of that hand-off: the maximum, its CTA count the word
+    // after it (0, or 4 for the columnwise half of a both-orientation call)
+    uint32_t amax_word;
     // grouped rowwise scaling: n_groups row ranges [offs[g], offs[g+1]), each
     // with its own amax / global scale (amax[g] final before the encode)
     const int64_t *group_offsets;
@@ -60,6 +63,11 @@ bool make_tmap_2d(CUtensorMap *map, const void *x, int elem_bytes, int64_t rows,
 // otherwise leaves the maximum bits in the workspace for the quantize kernel
 // launched next with a.amax_in_ws set.
 cudaError_t launch_amax_tensor(const QArgs &a, bool fp32, bool rht, bool col, bool publish, cudaStream_t s);
+// RHT amax of bf16 column blocks through TMA, for the quantize kernels of a
+// consumer call: with_rows also reduces the row blocks in the same read (row
+// maximum in workspace word 0, column maximum in word 4); without, the column
+// maximum goes to word 0.
+cudaError_t launch_amax_cols(const QArgs &a, bool with_rows, cudaStream_t s);
 // Per-row amax of the rowwise orientation (one value per X row).
 cudaError_t launch_amax_rows(const QArgs &a, bool fp32, bool rht, cudaStream_t s);
 

@@ -103,7 +103,7 @@ __device__ __forceinline__ void publish_tensor_amax(const QArgs &a, uint32_t m, 
 __device__ __forceinline__ float tensor_amax_read(const QArgs &a, bool rht) {
     if (!a.amax_in_ws) return a.amax[0];
     uint32_t bits;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(bits) : "l"(a.workspace) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(bits) : "l"(a.workspace + a.amax_word) : "memory");
     const float m = __uint_as_float(bits);
     return rht ? __fmul_rn(m, 0.25f) : m;
 }
@@ -116,10 +116,11 @@ __device__ __forceinline__ void tensor_amax_done(const QArgs &a, float A, float 
     if (threadIdx.x != 0) return;
     if (a.amax_in_ws) {
         uint32_t n;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(n) : "l"(a.workspace + 1) : "memory");
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(n) : "l"(a.workspace + a.amax_word + 1)
+                     : "memory");
         if (n == gridDim.x - 1) {
-            a.workspace[0] = 0u;
-            a.workspace[1] = 0u;
+            a.workspace[a.amax_word] = 0u;
+            a.workspace[a.amax_word + 1] = 0u;
         }
         if (blockIdx.x == 0) a.amax[0] = A;
     }

@@ -20,7 +20,7 @@ def swz(rows, cols):
     ("rowscaled_4o6_8192x8192", 8192 * 8192 * 2 + 8192 * 8192 // 2 + 8192 * 512 + 8 * 8192),
     # one read: the amax is given (read) and g written
     ("act_rht_sr_given_8192x4096", 8192 * 4096 * 2 + 8192 * 4096 // 2 + swz(8192, 4096) + 8),
-    # two reads (one amax pass could serve both orientations), both outputs, two amax/g pairs
+    # two reads (one amax pass serves both orientations), both outputs, two amax/g pairs
     ("act_rht_sr_rowcol_8192x4096", 2 * 8192 * 4096 * 2 + 16 + 2 * (8192 * 4096 // 2) + swz(8192, 4096)
      + swz(4096, 8192)),
     # two reads, 8 B per group (8 groups)
@@ -34,10 +34,10 @@ def test_counted_bytes(name, total):
     ("randn_rne_256x1024", ["k_quant_row_fused"]),
     ("act_rht_sr_8192x4096", ["k_amax_tma", "k_quant_row"]),
     ("weight_2d_rne_14336x4096", ["k_amax_tma", "k_quant_2d"]),
-    ("grad_col_rht_sr_16384x8192", ["k_amax_rht_col", "k_quant_col"]),
+    ("grad_col_rht_sr_16384x8192", ["k_amax_tma_cols", "k_quant_col"]),
     ("rowscaled_4o6_8192x8192", ["k_quant_rowscaled_staged"]),
     ("act_rht_sr_given_8192x4096", ["k_quant_row"]),
-    ("act_rht_sr_rowcol_8192x4096", ["k_amax_tma", "k_quant_row", "k_amax_rht_col", "k_quant_col"]),
+    ("act_rht_sr_rowcol_8192x4096", ["k_amax_tma_cols", "k_quant_row", "k_quant_col"]),
     ("act_rht_sr_groups_8192x4096", ["k_amax_groups", "k_group_finalize", "k_quant_rowscaled_staged"]),
 ])
 def test_call_kernels(name, kernels):
