@@ -245,6 +245,9 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         flush.fill_(k & 0xFF)  # evicts everything
         scrub.max()  # write-back of the dirty flush lines happens here, untimed
     amax_kernel, quant_kernel = kernel_plan(w)
+    # the split loop's amax pass is the standalone entry point: for RHT column
+    # blocks its kernel differs from the call's one-read pass
+    split_amax = "k_amax_rht_col" if (w.rht and w.colwise and not w.rowwise) else amax_kernel
     # two kernels: amax pass then encode, also timed separately (a two-scale
     # call runs four kernels and is timed as one call)
     split = amax_kernel is not None and not multi_kernel_call(w)
@@ -349,7 +352,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     peak, peak_src = hbm_peak()
     k1, k2 = statistics.mean(k1_ms), statistics.mean(k2_ms)
     if split and k1 > k2:
-        dom, dom_bytes, dom_ms, unit_desc = amax_kernel, nbytes["amax_pass"], k1, "2 B read per element"
+        dom, dom_bytes, dom_ms, unit_desc = split_amax, nbytes["amax_pass"], k1, "2 B read per element"
     elif split:
         dom, dom_bytes, dom_ms = quant_kernel, nbytes["quantize"], k2
         unit_desc = "2 B read + 0.5 B codes + 1/16 B scale per element (+ scale words)"
@@ -388,16 +391,24 @@ def run_ours(args, rank: int, world: int) -> dict | None:
                     "instructions_source": f"ncu smsp__inst_executed.sum per element, profiles/{dom}__{w.name}.md",
                     "ms_per_launch": round(dom_ms, 5), "hbm_view": {k: hbm_view[k] for k in
                                                                      ("achieved", "peak", "unit", "frac")}}
+    med = statistics.median(step_ms)
+    cfg = bench_config(w, world)
+    cfg["input_sha256"] = hashlib.sha256(x_cpu.contiguous().view(torch.int16).numpy().tobytes()).hexdigest()
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": bench_config(w, world),
+        "config": cfg,
+        # this rank's median step beside the mean (CUDA event ticks are ~2 us apart on this GPU: the mean
+        # over many steps resolves finer than any single step)
+        "ms_per_step_median": round(med, 5), "value_median": round(aggregate_gbs(nbytes["total"], med, world), 1),
+        "torch": torch.__version__,
         "counted_bytes_per_step": nbytes["total"],
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": roofline,
-        "kernels_ms": ({amax_kernel: round(k1, 5), quant_kernel: round(k2, 5), "split_step": round(split_ms, 5),
-                        "source": "second loop, event between the passes"} if split else
+        "kernels_ms": ({split_amax: round(k1, 5), quant_kernel: round(k2, 5), "split_step": round(split_ms, 5),
+                        "source": "second loop: the standalone amax pass, an event, the encode with the amax given"}
+                       if split else
                        {"call": round(k2, 5), "source": f"the timed steps ({len(call_kernels(w))} kernels per call)"}
                        if multi_kernel_call(w) else
                        {quant_kernel: round(k2, 5), "source": "the timed steps (one kernel per call)"}),
@@ -469,26 +480,51 @@ def pad_launch_needed(w: wl.Workload) -> bool:
 
 
 # ------------------------------------------------------------ the oracle
-def oracle_sample(w: wl.Workload, x_cpu: torch.Tensor, mask: int, rows: int, amax: float | None = None):
+def oracle_sample(w: wl.Workload, x_cpu: torch.Tensor, mask: int, rows: int, amax: float | None = None,
+                  threads: int = 1):
     """One oracle pass (amax + encode; the encode alone with a given amax)
-    over the first `rows` rows."""
+    over the first `rows` rows, single-threaded or over `threads` host threads
+    (row ranges; the same result bit for bit)."""
     import numpy as np
 
     import oracle
     xs = x_cpu[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    par = threads > 1
     if w.groups:  # each group (clipped to the sample) is its own tensor: amax, then encode
         for o0, o1 in zip(w.groups[:-1], w.groups[1:]):
             o1 = min(o1, rows)
             if o0 >= o1:
                 continue
-            A, _ = oracle.amax(xs[o0:o1], rht=w.rht, sign_mask=mask)
-            oracle.quantize(xs, mode=w.mode, swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed,
-                            offset=w.philox_offset, row_range=(o0, o1), amax_given=float(A[0]))
+            kw = dict(mode=w.mode, swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed,
+                      offset=w.philox_offset, row_range=(o0, o1))
+            if par:
+                A = oracle.amax_parallel(xs[o0:o1], rht=w.rht, sign_mask=mask, threads=threads)
+                oracle.quantize_parallel(xs, threads=threads, amax_given=A, **kw)
+            else:
+                A, _ = oracle.amax(xs[o0:o1], rht=w.rht, sign_mask=mask)
+                oracle.quantize(xs, amax_given=float(A[0]), **kw)
         return
     for colwise in ([False] if w.rowwise else []) + ([True] if w.colwise else []):
-        oracle.quantize(xs, colwise=colwise, mode=w.mode, block2d=w.block2d, per_row=w.per_row,
-                        swizzled=w.swizzled, rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset,
-                        amax_given=amax)
+        kw = dict(colwise=colwise, mode=w.mode, block2d=w.block2d, per_row=w.per_row, swizzled=w.swizzled,
+                  rht=w.rht, sign_mask=mask, seed=w.philox_seed, offset=w.philox_offset, amax_given=amax)
+        if par:
+            oracle.quantize_parallel(xs, threads=threads, **kw)
+        else:
+            oracle.quantize(xs, **kw)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
 
 
 def given_amax(w: wl.Workload, x_cpu: torch.Tensor, mask: int) -> float | None:
@@ -502,22 +538,33 @@ def given_amax(w: wl.Workload, x_cpu: torch.Tensor, mask: int) -> float | None:
     return float(oracle.amax(xs, colwise=w.colwise and not w.rowwise, rht=w.rht, sign_mask=mask)[0][0])
 
 
-def cpu_baseline(w: wl.Workload, x_cpu: torch.Tensor, mask: int, min_seconds: float) -> dict:
-    import oracle
-    oracle.build()
-    A = given_amax(w, x_cpu, mask)
+def timed_passes(w, x_cpu, mask, A, threads, min_seconds):
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle_sample(w, x_cpu, mask, w.rows, A)
+        oracle_sample(w, x_cpu, mask, w.rows, A, threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds:
-            break
-    gbs = reps * counted_bytes(w)["total"] / el / 1e9
-    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} full pass(es) of the {w.rows}x{w.cols} workload, single-threaded C oracle, "
-                      f"{el:.1f} s"}
+            return reps, el
+
+
+def cpu_baseline(w: wl.Workload, x_cpu: torch.Tensor, mask: int, min_seconds: float) -> dict:
+    """The oracle as it stands on the host: over all host cores (row ranges on
+    threads, bit-identical to one thread), and single-threaded beside it."""
+    import oracle
+    oracle.build()
+    A = given_amax(w, x_cpu, mask)
+    n = oracle.host_threads()
+    reps, el = timed_passes(w, x_cpu, mask, A, n, min_seconds / 2)
+    reps1, el1 = timed_passes(w, x_cpu, mask, A, 1, min_seconds / 2)
+    total = counted_bytes(w)["total"]
+    return {"value": round(reps * total / el / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{reps} full pass(es) of the {w.rows}x{w.cols} workload, C oracle on {n} host threads "
+                      f"(row ranges), {el:.1f} s",
+            "single_thread": {"value": round(reps1 * total / el1 / 1e9, 4), "cores": 1,
+                              "sample": f"{reps1} full pass(es), one thread, {el1:.1f} s"},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args) -> dict:
@@ -525,24 +572,27 @@ def run_reference(args) -> dict:
     oracle.build()
     w = wl.WORKLOADS[args.workload]
     x_cpu, mask = wl.make_input(w)
-    rows = 1024 if w.rows >= 1024 else w.rows
+    rows = min(w.rows, 4096)  # a bounded sample: the first rows of the workload
     sub = wl.Workload(**{**w.__dict__, "rows": rows})
     A = given_amax(w, x_cpu, mask)
+    n = oracle.host_threads()
     for _ in range(args.warmup):
-        oracle_sample(w, x_cpu, mask, rows, A)
+        oracle_sample(w, x_cpu, mask, rows, A, n)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_sample(w, x_cpu, mask, rows, A)
+        oracle_sample(w, x_cpu, mask, rows, A, n)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     v = counted_bytes(sub)["total"] / (ms * 1e-3) / 1e9
-    sample = f"rows 0..{rows} of the {w.rows}x{w.cols} workload per step (amax + encode), single-threaded C oracle"
+    sample = (f"rows 0..{rows} of the {w.rows}x{w.cols} workload per step (amax + encode), C oracle on {n} host "
+              f"threads (row ranges)")
     return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
             "config": bench_config(w, 1),
-            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

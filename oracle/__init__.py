@@ -15,6 +15,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -140,6 +141,86 @@ def quantize(x: np.ndarray, *, colwise: bool = False, mode: str = "rne", block2d
     if not swizzled:
         scales = scales.reshape(R, C // 16)
     return {"codes": codes, "scales": scales, "amax": amax, "global_scale": gs}
+
+
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def amax_parallel(x: np.ndarray, *, colwise: bool = False, rht: bool = False, sign_mask: int = 0,
+                  threads: int | None = None) -> float:
+    """The per-tensor amax of ``amax`` computed on slices in parallel threads:
+    row ranges for rowwise blocks, column ranges for columnwise ones (so every
+    block lies in one slice), combined by the same unsigned maximum of magnitude
+    bits, hence equal to the single call bit for bit (NaN included)."""
+    x, _, _ = _input(x)
+    rows, cols = x.shape
+    n = max(1, min(threads or host_threads(), (cols if colwise else rows)))
+    cuts = np.linspace(0, cols if colwise else rows, n + 1).astype(int)
+
+    def one(i):
+        part = x[:, cuts[i]:cuts[i + 1]] if colwise else x[cuts[i]:cuts[i + 1]]
+        return amax(part, colwise=colwise, rht=rht, sign_mask=sign_mask)[0]
+
+    with ThreadPoolExecutor(n) as ex:
+        parts = [p for p in ex.map(one, range(n)) if p.size]
+    bits = max(int(p.view(np.uint32)[0]) & 0x7FFFFFFF for p in parts)
+    return float(np.array([bits], np.uint32).view(np.float32)[0])
+
+
+def quantize_parallel(x: np.ndarray, *, threads: int | None = None, colwise: bool = False, mode: str = "rne",
+                      block2d: bool = False, per_row: bool = False, swizzled: bool = False, rht: bool = False,
+                      sign_mask: int = 0, seed: int = 0, offset: int = 0,
+                      amax_given: float | None = None, row_range: tuple[int, int] | None = None) -> dict:
+    """``quantize`` of the whole tensor with its output rows split over threads.
+
+    Orchestration only (the arithmetic is the same C code): the per-tensor
+    amax comes from ``amax_parallel`` (or ``amax_given``), then each thread
+    encodes a range of output rows into the shared code and scale arrays (whole
+    16-row bands in 2D mode; only ``row_range`` if given, as ``quantize``).  An
+    output row depends only on the input, the global scale and its own Philox
+    blocks, so the result equals a single call bit for bit."""
+    x, dtype, ld = _input(x)
+    rows, cols = x.shape
+    R, C = (cols, rows) if colwise else (rows, cols)
+    n = threads or host_threads()
+    if not per_row and amax_given is None:
+        amax_given = amax_parallel(x, colwise=colwise, rht=rht, sign_mask=sign_mask, threads=n)
+    codes = np.zeros((R, C // 2), np.uint8)
+    scales = np.zeros(scale_bytes(R, C, swizzled), np.uint8)
+    n_g = R if per_row else 1
+    amax_out = np.zeros(n_g, np.float32)
+    gs_out = np.zeros(n_g, np.float32)
+    step = 16 if block2d else 1
+    lo, hi = row_range if row_range is not None else (0, R)
+    units = (hi - lo) // step
+    cuts = (lo + np.linspace(0, units, max(1, min(units, 4 * n)) + 1).astype(int) * step).tolist()
+    given = None if amax_given is None else np.array([amax_given], np.float32)
+    lib = _lib()
+
+    def one(i):
+        r0, r1 = cuts[i], cuts[i + 1]
+        a, g = (amax_out, gs_out) if per_row else (np.zeros(1, np.float32), np.zeros(1, np.float32))
+        rc = lib.ora_quantize(_ptr(x), dtype, rows, cols, ld, int(colwise), MODES[mode], int(block2d),
+                              int(per_row), int(swizzled), int(rht), sign_mask & 0xFFFF, seed, offset,
+                              r0, r1, None if given is None else _ptr(given),
+                              _ptr(codes), _ptr(scales), _ptr(a), _ptr(g))
+        return rc, a, g
+
+    with ThreadPoolExecutor(n) as ex:
+        results = list(ex.map(one, range(len(cuts) - 1)))
+    for rc, _, _ in results:
+        if rc != 0:
+            raise ValueError(f"oracle quantize rejected the arguments (status {rc})")
+    if not per_row:
+        amax_out[:], gs_out[:] = results[0][1], results[0][2]
+    if not swizzled:
+        scales = scales.reshape(R, C // 16)
+    return {"codes": codes, "scales": scales, "amax": amax_out, "global_scale": gs_out}
 
 
 def dequantize(codes: np.ndarray, scales: np.ndarray, global_scale: np.ndarray, rows: int, cols: int,

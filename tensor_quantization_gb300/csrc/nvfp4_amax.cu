@@ -64,9 +64,9 @@ static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "
 // cannot change the result.  In a quantize call the CTAs fold their running
 // maximum into the workspace word once per tile and read it back (one tile
 // late), so after the first tiles most blocks cost a bit-max instead of a
-// butterfly; the result is the same maximum, bit for bit.  Only thread 0 of a
-// CTA sends to the workspace word, so in the standalone pass its last hint
-// precedes its ticket, and the last ticket's reset comes after every hint.
+// butterfly; the result is the same maximum, bit for bit.  (The standalone
+// pass transforms every block: there the shared hint measured 2 us slower on
+// 8192x4096, with the tile counter's traffic beside it.)
 constexpr bool kAmaxSkip = true;
 
 // A known lower bound of the tensor maximum for the skip test, shared through
@@ -114,7 +114,7 @@ template <bool RHT, typename T, bool PUBLISH>
 __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_constant__ CUtensorMap tmap,
                                                               const QArgs a) {
     using ST = StreamTile<T>;
-    constexpr bool SKIP = RHT && kAmaxSkip;
+    constexpr bool SKIP = RHT && !PUBLISH && kAmaxSkip;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full[kStreamStages];
     __shared__ __align__(8) uint64_t empty[kStreamStages];
@@ -205,12 +205,11 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
 // k_amax_tma does, so both orientations' maxima come from one read of the
 // input (the operand of a weight-gradient GEMM needs both).  Both use the
 // skip test above.  The column maximum goes to workspace word kColWord (4)
-// when ROW is set, else to word 0; the row maximum to word 0.  PUBLISH (the
-// standalone pass, columns only): the last CTA publishes amax and g.
-template <bool ROW, bool PUBLISH>
+// when ROW is set, else to word 0; the row maximum to word 0.  Consumer calls
+// only: the quantize kernels publish.
+template <bool ROW>
 __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma_cols(const __grid_constant__ CUtensorMap tmap,
                                                                    const QArgs a) {
-    static_assert(!(ROW && PUBLISH), "the two-orientation pass hands its maxima to quantize kernels");
     using T = bf16_t;
     using ST = StreamTile<T>;
     constexpr uint32_t kColWord = ROW ? 4u : 0u;
@@ -291,10 +290,6 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma_cols(const __grid_
     if (!ok) {  // a bounded wait gave up: record it, and NaN maxima poison both scales
         wait_gave_up(a, nullptr);
         mr = mc = 0x7FFFFFFFu;
-    }
-    if (PUBLISH) {
-        publish_tensor_amax(a, mc, true);
-        return;
     }
     allow_dependents();  // the quantize kernel may start staging its tiles
     mr = __reduce_max_sync(0xFFFFFFFFu, mr);
@@ -457,9 +452,9 @@ static cudaError_t run_amax_tma(const QArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <bool ROW, bool PUBLISH>
+template <bool ROW>
 static cudaError_t run_amax_tma_cols(const QArgs &a, cudaStream_t s) {
-    auto k = k_amax_tma_cols<ROW, PUBLISH>;
+    auto k = k_amax_tma_cols<ROW>;
     constexpr int smem = StreamTile<bf16_t>::kSmemBytes;
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
@@ -482,14 +477,13 @@ static cudaError_t run_amax_tma_cols(const QArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_amax_cols(const QArgs &a, bool with_rows, cudaStream_t s) {
-    return with_rows ? run_amax_tma_cols<true, false>(a, s) : run_amax_tma_cols<false, false>(a, s);
+    return with_rows ? run_amax_tma_cols<true>(a, s) : run_amax_tma_cols<false>(a, s);
 }
 
 template <typename T, bool PUBLISH>
 static cudaError_t run_amax_tensor(const QArgs &a, bool rht, bool col, cudaStream_t s) {
     constexpr int W = Chunk<T>::W;
     if (!col) return rht ? run_amax_tma<true, T, PUBLISH>(a, s) : run_amax_tma<false, T, PUBLISH>(a, s);
-    if (PUBLISH && sizeof(T) == 2) return run_amax_tma_cols<false, true>(a, s);
     auto k = k_amax_rht_col<T, PUBLISH>;
     k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
     return cudaGetLastError();

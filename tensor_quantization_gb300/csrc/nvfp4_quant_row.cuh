@@ -186,16 +186,18 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
                                                      (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
                     }
                 }
-                // blocks past the last column arrive zero-filled and encode as
-                // zeros that are not stored: no per-block branch
+                // (encoding the zero-filled blocks past the last column instead of
+                // branching around them measured 1 us slower per 8192x4096 call)
 #pragma unroll
                 for (int b = 0; b < 4; b++) {
-                    RawBlock<T> raw;
-                    stage_block<T>(stage, tid, b, raw);
-                    f2 v[8];
-                    if (RHT) unpack_fwht_first(raw, v);
-                    else unpack(raw, v);
-                    c[b] = encode_block_fast<MODE, RHT, AP, true, true>(v, sd, tab, signs, rnd[b], S[b]);
+                    if (j0 + b < CS) {
+                        RawBlock<T> raw;
+                        stage_block<T>(stage, tid, b, raw);
+                        f2 v[8];
+                        if (RHT) unpack_fwht_first(raw, v);
+                        else unpack(raw, v);
+                        c[b] = encode_block_fast<MODE, RHT, AP, true, true>(v, sd, tab, signs, rnd[b], S[b]);
+                    }
                 }
             } else {
 #pragma unroll

@@ -92,6 +92,33 @@ def oracle_run(x_cpu: torch.Tensor, *, mode="rne", rowwise=True, colwise=False, 
     return out
 
 
+def oracle_run_all_cores(x_cpu: torch.Tensor, *, mode="rne", rowwise=True, colwise=False, block2d=False,
+                         per_row=False, swizzled=False, rht=False, sign_mask=0, seed=0, offset=0, amax=None) -> dict:
+    """oracle_run of the whole tensor on every host core (the oracle's row-range
+    threads; bit-identical to one thread)."""
+    xn = np_bits(x_cpu)
+    out, amaxes, scales = {}, [], []
+    for i, (orient, on) in enumerate((("row", rowwise), ("col", colwise))):
+        if not on:
+            continue
+        given = None
+        if amax is not None:
+            a = np.asarray(amax).ravel()
+            given = float(a[i if (rht and rowwise and colwise) else 0])
+        o = oracle.quantize_parallel(xn, colwise=orient == "col", mode=mode, block2d=block2d, per_row=per_row,
+                                     swizzled=swizzled, rht=rht, sign_mask=sign_mask, seed=seed, offset=offset,
+                                     amax_given=given)
+        out[f"codes_{orient}"] = o["codes"]
+        out[f"scales_{orient}"] = o["scales"].ravel()
+        amaxes.append(o["amax"])
+        scales.append(o["global_scale"])
+    if rht and rowwise and colwise:
+        out["amax"], out["global_scale"] = np.concatenate(amaxes), np.concatenate(scales)
+    else:
+        out["amax"], out["global_scale"] = amaxes[-1], scales[-1]
+    return out
+
+
 def assert_parity(g: dict, o: dict, rows_sampled=None):
     for k in ("codes_row", "scales_row", "codes_col", "scales_col"):
         if k not in o:
@@ -151,46 +178,18 @@ def test_workload_small(name):
     assert_parity(gpu_run(x, **gkw), oracle_run(x, **okw))
 
 
-def bands(n: int) -> list[tuple[int, int]]:
-    return [(0, 256), (n // 2 - 128, n // 2 + 128), (n - 256, n)]
-
-
 @pytest.mark.slow
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
 def test_workload_full_size(name):
-    """Full-size workloads through the call bench.py times.  Workloads up to the
-    headline size compare every output; larger ones compare bands of output
-    rows spread over the tensor (the per-tensor amax always covers all of it)
-    plus, for swizzled layouts, every scale byte."""
+    """Full-size workloads through the call bench.py times, every output byte
+    compared with the oracle (run over all host cores)."""
     w = wl.WORKLOADS[name]
     if w.groups:
         pytest.skip("grouped: test_full_size_rht_both_orientations_and_groups covers this input with these group offsets")
     x, mask = wl.make_input(w)
     gkw, kw = workload_runs(w, x, mask)
     g = gpu_run(x, **gkw)
-    if w.numel <= 8192 * 4096:
-        assert_parity(g, oracle_run(x, **kw))
-        return
-    for orient in ("row", "col"):
-        if not (w.rowwise if orient == "row" else w.colwise):
-            continue
-        R_out, C_out = (w.rows, w.cols) if orient == "row" else (w.cols, w.rows)
-        okw = dict(kw, rowwise=orient == "row", colwise=orient == "col")
-        for r0, r1 in bands(R_out):
-            o = oracle_run(x, row_range=(r0, r1), **okw)
-            ck, sk = f"codes_{orient}", f"scales_{orient}"
-            assert np.array_equal(g[ck][r0:r1], o[ck][r0:r1]), (name, ck, r0)
-            if not w.swizzled:
-                assert np.array_equal(g[sk].reshape(R_out, -1)[r0:r1], o[sk].reshape(R_out, -1)[r0:r1])
-            if w.per_row:
-                assert same_float_bits(g["amax"][r0:r1], o["amax"][r0:r1])
-                assert same_float_bits(g["global_scale"][r0:r1], o["global_scale"][r0:r1])
-            else:
-                assert same_float_bits(g["amax"], o["amax"])
-                assert same_float_bits(g["global_scale"], o["global_scale"])
-        if w.swizzled:
-            o = oracle_run(x, **okw)
-            assert np.array_equal(g[f"scales_{orient}"], o[f"scales_{orient}"]), name
+    assert_parity(g, oracle_run_all_cores(x, **kw))
     if w.block2d:
         # 2D: the column codes are the nibble transpose of the row codes
         cr, cc = g["codes_row"], g["codes_col"]
@@ -717,34 +716,30 @@ def test_rht_round_trip_through_the_library():
 
 @pytest.mark.slow
 def test_full_size_rht_both_orientations_and_groups():
-    """The headline activation (8192x4096) in both orientations with the RHT, and
-    as 8 row groups of uneven sizes, compared in row bands with the oracle."""
+    """The headline activation (8192x4096) in both orientations with the RHT
+    (linear scales), and as 8 row groups of uneven sizes (an empty and a
+    one-row group among them), every output compared with the oracle."""
     w = wl.WORKLOADS["act_rht_sr_8192x4096"]
     x, mask = wl.make_input(w)
     kw = dict(mode="sr", rht=True, rowwise=True, colwise=True, swizzled=False, sign_mask=mask, seed=1)
-    g = gpu_run(x, **kw)
-    for orient, R_out in (("row", 8192), ("col", 4096)):
-        okw = dict(kw, rowwise=orient == "row", colwise=orient == "col")
-        for r0, r1 in bands(R_out):
-            o = oracle_run(x, row_range=(r0, r1), **okw)
-            assert np.array_equal(g[f"codes_{orient}"][r0:r1], o[f"codes_{orient}"][r0:r1]), (orient, r0)
-            assert np.array_equal(g[f"scales_{orient}"].reshape(R_out, -1)[r0:r1],
-                                  o[f"scales_{orient}"].reshape(R_out, -1)[r0:r1])
-        idx = 0 if orient == "row" else 1
-        assert same_float_bits(g["amax"][idx:idx + 1], o["amax"])
+    assert_parity(gpu_run(x, **kw), oracle_run_all_cores(x, **kw))
     offs = [0, 100, 1124, 1124, 4000, 4001, 6000, 7999, 8192]
     q = nvfp4.quantize_grouped(to_device(x), torch.tensor(offs, dtype=torch.int64, device="cuda"), mode="rht_sr",
-                               sign_mask=mask, seed=1)
+                               sign_mask=mask, seed=1, swizzled=True)
     torch.cuda.synchronize()
     xn = np_bits(x)
-    for gi in (0, 1, 4, 6):
+    codes, scales = np.zeros((8192, 2048), np.uint8), np.zeros(8192 * 256, np.uint8)
+    for gi in range(len(offs) - 1):
         o0, o1 = offs[gi], offs[gi + 1]
-        A, _ = oracle.amax(xn[o0:o1], rht=True, sign_mask=mask)
-        r1 = min(o1, o0 + 64)
-        o = oracle.quantize(xn, mode="sr", rht=True, sign_mask=mask, seed=1, row_range=(o0, r1),
-                            amax_given=float(np.asarray(A).ravel()[0]))
-        assert np.array_equal(q.codes_row[o0:r1].cpu().numpy(), o["codes"][o0:r1]), gi
-        assert same_float_bits(q.amax[gi:gi + 1].cpu().numpy(), np.asarray(A).ravel())
+        A = oracle.amax_parallel(xn[o0:o1], rht=True, sign_mask=mask) if o1 > o0 else 0.0
+        if o1 > o0:
+            o = oracle.quantize_parallel(xn, mode="sr", rht=True, sign_mask=mask, seed=1, swizzled=True,
+                                         row_range=(o0, o1), amax_given=A)
+            codes[o0:o1] = o["codes"][o0:o1]
+            scales |= o["scales"]  # each group writes its own rows' scale bytes, the rest stay 0
+        assert same_float_bits(q.amax[gi:gi + 1].cpu().numpy(), np.float32([A]))
+    assert np.array_equal(q.codes_row.cpu().numpy(), codes)
+    assert np.array_equal(q.scales_row.cpu().numpy(), scales)
 
 
 def test_calls_on_two_streams_at_once():
