@@ -245,9 +245,9 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         flush.fill_(k & 0xFF)  # evicts everything
         scrub.max()  # write-back of the dirty flush lines happens here, untimed
     amax_kernel, quant_kernel = kernel_plan(w)
-    # the split loop's amax pass is the standalone entry point: for RHT column
-    # blocks its kernel differs from the call's one-read pass
-    split_amax = "k_amax_rht_col" if (w.rht and w.colwise and not w.rowwise) else amax_kernel
+    # the split loop's amax pass is the standalone entry point, whose kernel
+    # differs from the call's with the RHT
+    split_amax = ("k_amax_rht_col" if w.colwise else "k_amax_tma") if w.rht else amax_kernel
     # two kernels: amax pass then encode, also timed separately (a two-scale
     # call runs four kernels and is timed as one call)
     split = amax_kernel is not None and not multi_kernel_call(w)
@@ -447,8 +447,9 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
         return None, ("k_quant_2d" if w.block2d else "k_quant_col" if not w.rowwise else "k_quant_row")
     if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
         return None, "k_quant_row_fused"
-    # bf16 RHT column blocks (alone, or with the row blocks of the same read)
-    amax = "k_amax_tma_cols" if (w.rht and w.colwise) else "k_amax_tma"
+    # bf16 RHT column blocks (alone, or with the row blocks of the same read);
+    # RHT row blocks of a contiguous bf16 input: the load-based pass
+    amax = "k_amax_tma_cols" if (w.rht and w.colwise) else "k_amax_ldg_rht" if w.rht else "k_amax_tma"
     if w.block2d:
         return amax, "k_quant_2d"
     if w.colwise and not w.rowwise:

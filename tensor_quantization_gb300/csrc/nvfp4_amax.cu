@@ -196,6 +196,55 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
     else fold_tensor_amax_warps(a, m, &warp_max, &warps_in);
 }
 
+// RHT amax of contiguous bf16 rows (row pitch = row length) for a quantize
+// call, with plain 16-byte loads: the tensor is one run of 1x16 blocks, block
+// i at element 16 i; each thread keeps kLdgBlocks blocks (128 bytes) in flight
+// and a warp's loads of one round cover 1 KiB contiguously.  Same skip test
+// and hand-off as k_amax_tma.  The loop that folds the hint runs a
+// warp-uniform number of rounds (the tail rounds follow without it).
+constexpr int kLdgBlocks = 4;
+constexpr int kAmaxLdgThreads = 256;
+
+__global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_ldg_rht(const QArgs a) {
+    __shared__ uint32_t warp_max, warps_in, hint_words[2];
+    if (threadIdx.x == 0) {
+        warp_max = 0u;
+        warps_in = 0u;
+        hint_words[0] = hint_words[1] = 0u;
+    }
+    __syncthreads();
+    const bf16_t *x = static_cast<const bf16_t *>(a.x);
+    const uint64_t nblk = (uint64_t)a.rows * (uint64_t)(a.cols >> 4);
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint32_t lane = threadIdx.x & 31;
+    uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    MaxHint hint(&hint_words[0], &hint_words[1], a.workspace);
+    uint32_t m = 0;
+    auto reduce = [&](const RawBlock<bf16_t> &raw) {
+        if (!kAmaxSkip || butterfly_bound(raw) > hint.threshold(m)) {
+            f2 v[8];
+            unpack(raw, v);
+            fwht16(v);
+            m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+        }
+    };
+    // full rounds: the warp's last lane still has kLdgBlocks blocks
+    for (; i - lane + 31 + (kLdgBlocks - 1) * stride < nblk; i += kLdgBlocks * stride) {
+        RawBlock<bf16_t> raw[kLdgBlocks];
+#pragma unroll
+        for (int u = 0; u < kLdgBlocks; u++) load_raw(x + (i + u * stride) * 16, raw[u]);
+#pragma unroll
+        for (int u = 0; u < kLdgBlocks; u++) reduce(raw[u]);
+        if (kAmaxSkip) hint.fold(m);
+    }
+    for (; i < nblk; i += stride) {
+        RawBlock<bf16_t> raw;
+        load_raw(x + i * 16, raw);
+        reduce(raw);
+    }
+    fold_tensor_amax_warps(a, m, &warp_max, &warps_in);
+}
+
 // RHT blocks along the columns (16 rows of one column), and optionally the
 // row blocks too, from one TMA stream of the bf16 input (the tiles and stages
 // of k_amax_tma).  A warp takes a 16-row strip of the tile and each lane two
@@ -476,6 +525,22 @@ static cudaError_t run_amax_tma_cols(const QArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The load-based pass replaces the TMA one for contiguous bf16 rows in a
+// quantize call.
+constexpr bool kAmaxLdg = true;
+
+static cudaError_t run_amax_ldg_rht(const QArgs &a, cudaStream_t s) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_amax_ldg_rht, kAmaxLdgThreads, 0);
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 4) per_sm = 4;
+    const int64_t nblk = a.rows * (a.cols >> 4);
+    const int64_t want = (nblk + kAmaxLdgThreads - 1) / kAmaxLdgThreads;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    k_amax_ldg_rht<<<(int)(want < cap ? want : cap), kAmaxLdgThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_amax_cols(const QArgs &a, bool with_rows, cudaStream_t s) {
     return with_rows ? run_amax_tma_cols<true>(a, s) : run_amax_tma_cols<false>(a, s);
 }
@@ -483,6 +548,7 @@ cudaError_t launch_amax_cols(const QArgs &a, bool with_rows, cudaStream_t s) {
 template <typename T, bool PUBLISH>
 static cudaError_t run_amax_tensor(const QArgs &a, bool rht, bool col, cudaStream_t s) {
     constexpr int W = Chunk<T>::W;
+    if (kAmaxLdg && !PUBLISH && rht && !col && sizeof(T) == 2 && a.ld == a.cols) return run_amax_ldg_rht(a, s);
     if (!col) return rht ? run_amax_tma<true, T, PUBLISH>(a, s) : run_amax_tma<false, T, PUBLISH>(a, s);
     auto k = k_amax_rht_col<T, PUBLISH>;
     k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);

@@ -32,7 +32,7 @@ def test_counted_bytes(name, total):
 
 @pytest.mark.parametrize("name,kernels", [
     ("randn_rne_256x1024", ["k_quant_row_fused"]),
-    ("act_rht_sr_8192x4096", ["k_amax_tma", "k_quant_row"]),
+    ("act_rht_sr_8192x4096", ["k_amax_ldg_rht", "k_quant_row"]),
     ("weight_2d_rne_14336x4096", ["k_amax_tma", "k_quant_2d"]),
     ("grad_col_rht_sr_16384x8192", ["k_amax_tma_cols", "k_quant_col"]),
     ("rowscaled_4o6_8192x8192", ["k_quant_rowscaled_staged"]),
