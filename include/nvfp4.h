@@ -212,8 +212,8 @@ nvfp4_status nvfp4_quantize_rht_sr(const nvfp4_input *in, uint32_t flags, uint16
  * the implicit device synchronisation an allocation can cause.  It allocates
  * nothing (no cudaMalloc, cudaFree or allocating library routine): the amax
  * pass's scratch lives in a 256-byte device array inside the library, which
- * every GPU that loads the library keeps until the process exits.  The pass
- * needs 12 of those bytes for any input size; the call returns
+ * every GPU that loads the library keeps until the process exits.  The passes
+ * need at most 24 of those bytes for any input size; the call returns
  * NVFP4_ERR_UNSUPPORTED if the library's workspace need ever exceeds the array.
  * Inputs and outputs are as for nvfp4_quantize_rht_sr, whose checks (sizes
  * included) apply unchanged.
