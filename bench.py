@@ -597,6 +597,110 @@ def run_reference(args) -> dict:
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------- the read-bandwidth bound
+READ_PROBE_SRC = r"""
+#include <cstdint>
+#include <cuda_runtime.h>
+// every thread keeps U 16-byte loads in flight; the maximum of an xor of each
+// word keeps the loads live; one atomicMax per warp
+template <int U>
+__global__ void read_max(const uint4 *p, long long n, unsigned *out) {
+    unsigned m = 0;
+    long long i = (long long)blockIdx.x * blockDim.x * U + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x * U;
+    for (; i + (long long)(U - 1) * blockDim.x < n; i += stride) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; u++)
+            asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w) : "l"(p + i + u * blockDim.x));
+#pragma unroll
+        for (int u = 0; u < U; u++) m = max(m, v[u].x ^ v[u].y ^ v[u].z ^ v[u].w);
+    }
+    for (; i < n; i += blockDim.x) { uint4 v = p[i]; m = max(m, v.x ^ v.y ^ v.z ^ v.w); }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) atomicMax(out, m);
+}
+extern "C" int read_probe(const void *p, long long bytes, unsigned *out, int ctas_per_sm, int in_flight,
+                          void *stream) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (in_flight == 8) read_max<8><<<sms * ctas_per_sm, 256, 0, s>>>((const uint4 *)p, bytes / 16, out);
+    else read_max<4><<<sms * ctas_per_sm, 256, 0, s>>>((const uint4 *)p, bytes / 16, out);
+    return (int)cudaGetLastError();
+}
+"""
+
+
+def read_sweep(args) -> dict:
+    """Event time of a plain read of N MiB right after the bench's L2 flush (the
+    bound of any pass that must read the input from HBM), beside the library's
+    standalone amax passes on the headline input."""
+    import subprocess
+    import tempfile
+
+    from tensor_quantization_gb300 import build, nvfp4
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    nvfp4.load()
+    tmp = tempfile.mkdtemp()
+    with open(os.path.join(tmp, "read_probe.cu"), "w") as f:
+        f.write(READ_PROBE_SRC)
+    so = os.path.join(tmp, "libread_probe.so")
+    subprocess.run([build.nvcc(), *build.ARCH, "-O3", "-Xcompiler", "-fPIC", "-shared",
+                    os.path.join(tmp, "read_probe.cu"), "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    lib.read_probe.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_void_p]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scrub = torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=dev)
+    buf = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    out = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def timed(call, reps):
+        ts = []
+        for k in range(reps + 3):
+            flush.fill_(k & 0xFF)
+            scrub.max()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            e1.synchronize()
+            if k >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return ts
+
+    rows = []
+    with ClockSampler(0) as clk:
+        for ctas, fl in ((4, 8), (8, 4)):
+            for mib in (16, 32, 64, 128, 256):
+                ts = timed(lambda: lib.read_probe(ctypes.c_void_p(buf.data_ptr()), mib << 20,
+                                                  ctypes.c_void_p(out.data_ptr()), ctas, fl, st), args.steps)
+                m = statistics.mean(ts)
+                rows.append({"kernel": f"plain read, {ctas} CTAs x 256 threads per SM, {fl} x 16 B in flight",
+                             "mib": mib, "mean_us": round(m, 2), "median_us": round(statistics.median(ts), 2),
+                             "gbs": round((mib << 20) / m / 1e3, 1)})
+        w = wl.WORKLOADS[wl.HEADLINE]
+        x_cpu, mask = wl.make_input(w)
+        x = x_cpu.to(dev)
+        a = torch.empty(1, device=dev)
+        g = torch.empty(1, device=dev)
+        ws = torch.zeros(nvfp4.nvfp4_workspace_bytes(), dtype=torch.uint8, device=dev)
+        o = nvfp4.make_output(amax=a, global_scale=g)
+        for rht in (False, True):
+            ts = timed(lambda: nvfp4.nvfp4_amax(x, nvfp4.ROWWISE, rht, mask, o, ws), args.steps)
+            m = statistics.mean(ts)
+            rows.append({"kernel": f"nvfp4_amax standalone ({'RHT' if rht else 'no RHT'}), {w.name}", "mib": 64,
+                         "mean_us": round(m, 2), "median_us": round(statistics.median(ts), 2),
+                         "gbs": round((64 << 20) / m / 1e3, 1)})
+    return {"read_sweep": rows, "reps": args.steps, "clocks": clk.summary(),
+            "l2": "flushed before every call: 512 MiB write + 256 MiB read"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,7 +710,12 @@ def main():
     ap.add_argument("--workload", default=wl.HEADLINE, choices=list(wl.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (0 = skip)")
     ap.add_argument("--shape", default=None, help="ROWSxCOLS override of the workload's shape (profiling cases)")
+    ap.add_argument("--read-sweep", action="store_true",
+                    help="print the plain-read bound after the L2 flush (16..256 MiB) instead of the bench line")
     args = ap.parse_args()
+    if args.read_sweep:
+        print(json.dumps(read_sweep(args)), flush=True)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
