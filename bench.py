@@ -247,7 +247,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     amax_kernel, quant_kernel = kernel_plan(w)
     # the split loop's amax pass is the standalone entry point, whose kernel
     # differs from the call's with the RHT
-    split_amax = ("k_amax_rht_col" if w.colwise else "k_amax_tma") if w.rht else amax_kernel
+    split_amax = ("k_amax_rht_col" if w.colwise else "k_amax_ldg_rht") if w.rht else amax_kernel
     # two kernels: amax pass then encode, also timed separately (a two-scale
     # call runs four kernels and is timed as one call)
     split = amax_kernel is not None and not multi_kernel_call(w)

@@ -65,8 +65,8 @@ static_assert(kAmaxTmaThreads == 2 * kStreamTileRows && kStreamTileCols == 64, "
 // maximum into the workspace word once per tile and read it back (one tile
 // late), so after the first tiles most blocks cost a bit-max instead of a
 // butterfly; the result is the same maximum, bit for bit.  (The standalone
-// pass transforms every block: there the shared hint measured 2 us slower on
-// 8192x4096, with the tile counter's traffic beside it.)
+// TMA pass transforms every block: there the shared hint measured 2 us slower
+// on 8192x4096, with the tile counter's traffic beside it.)
 constexpr bool kAmaxSkip = true;
 
 // A known lower bound of the tensor maximum for the skip test, shared through
@@ -202,10 +202,15 @@ __global__ void __launch_bounds__(kAmaxTmaThreads) k_amax_tma(const __grid_const
 // and a warp's loads of one round cover 1 KiB contiguously.  Same skip test
 // and hand-off as k_amax_tma.  The loop that folds the hint runs a
 // warp-uniform number of rounds (the tail rounds follow without it).
+// PUBLISH (the standalone entry point): the last CTA publishes amax and g;
+// only thread 0 of a CTA sends hints to the workspace word, so every hint
+// precedes that CTA's ticket and the last ticket's reset follows them all.
 constexpr int kLdgBlocks = 4;
 constexpr int kAmaxLdgThreads = 256;
 
+template <bool PUBLISH>
 __global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_ldg_rht(const QArgs a) {
+    constexpr bool SKIP = kAmaxSkip;
     __shared__ uint32_t warp_max, warps_in, hint_words[2];
     if (threadIdx.x == 0) {
         warp_max = 0u;
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_ldg_rht(const QArgs a)
     MaxHint hint(&hint_words[0], &hint_words[1], a.workspace);
     uint32_t m = 0;
     auto reduce = [&](const RawBlock<bf16_t> &raw) {
-        if (!kAmaxSkip || butterfly_bound(raw) > hint.threshold(m)) {
+        if (!SKIP || butterfly_bound(raw) > hint.threshold(m)) {
             f2 v[8];
             unpack(raw, v);
             fwht16(v);
@@ -235,14 +240,15 @@ __global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_ldg_rht(const QArgs a)
         for (int u = 0; u < kLdgBlocks; u++) load_raw(x + (i + u * stride) * 16, raw[u]);
 #pragma unroll
         for (int u = 0; u < kLdgBlocks; u++) reduce(raw[u]);
-        if (kAmaxSkip) hint.fold(m);
+        if (SKIP) hint.fold(m);
     }
     for (; i < nblk; i += stride) {
         RawBlock<bf16_t> raw;
         load_raw(x + i * 16, raw);
         reduce(raw);
     }
-    fold_tensor_amax_warps(a, m, &warp_max, &warps_in);
+    if (PUBLISH) publish_tensor_amax(a, m, true);
+    else fold_tensor_amax_warps(a, m, &warp_max, &warps_in);
 }
 
 // RHT blocks along the columns (16 rows of one column), and optionally the
@@ -529,15 +535,17 @@ static cudaError_t run_amax_tma_cols(const QArgs &a, cudaStream_t s) {
 // quantize call.
 constexpr bool kAmaxLdg = true;
 
+template <bool PUBLISH>
 static cudaError_t run_amax_ldg_rht(const QArgs &a, cudaStream_t s) {
+    auto k = k_amax_ldg_rht<PUBLISH>;
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_amax_ldg_rht, kAmaxLdgThreads, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAmaxLdgThreads, 0);
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 4) per_sm = 4;
     const int64_t nblk = a.rows * (a.cols >> 4);
     const int64_t want = (nblk + kAmaxLdgThreads - 1) / kAmaxLdgThreads;
     const int64_t cap = (int64_t)sm_count() * per_sm;
-    k_amax_ldg_rht<<<(int)(want < cap ? want : cap), kAmaxLdgThreads, 0, s>>>(a);
+    k<<<(int)(want < cap ? want : cap), kAmaxLdgThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -548,7 +556,7 @@ cudaError_t launch_amax_cols(const QArgs &a, bool with_rows, cudaStream_t s) {
 template <typename T, bool PUBLISH>
 static cudaError_t run_amax_tensor(const QArgs &a, bool rht, bool col, cudaStream_t s) {
     constexpr int W = Chunk<T>::W;
-    if (kAmaxLdg && !PUBLISH && rht && !col && sizeof(T) == 2 && a.ld == a.cols) return run_amax_ldg_rht(a, s);
+    if (kAmaxLdg && rht && !col && sizeof(T) == 2 && a.ld == a.cols) return run_amax_ldg_rht<PUBLISH>(a, s);
     if (!col) return rht ? run_amax_tma<true, T, PUBLISH>(a, s) : run_amax_tma<false, T, PUBLISH>(a, s);
     auto k = k_amax_rht_col<T, PUBLISH>;
     k<<<grid_for(k, (a.rows >> 4) * ((a.cols + W - 1) / W)), 256, 0, s>>>(a);
