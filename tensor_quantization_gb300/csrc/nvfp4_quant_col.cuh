@@ -143,18 +143,72 @@ __device__ __forceinline__ void write_col_tile(const QArgs &a, const uint8_t *oc
     }
 }
 
+// Columnwise kernel: the TMA tiles and thread layout above, but a thread
+// encodes its HC columns two at a time (one 32-bit strip word per row for
+// bf16), and stores each block's 8 code bytes and its scale byte straight
+// from registers: the 16 lanes of a half warp write 16 different output rows,
+// and the eight row blocks of a tile complete each row's 64 contiguous bytes
+// while they sit in L2.  No shared output tile and half the strip live at a
+// time, so five CTAs fit per SM instead of four.  Pad bytes of a swizzled
+// scale layout are written by the pad kernel.
+template <typename T>
+struct ColStrip {  // the 16 rows of two adjacent columns of a thread's half chunk
+    uint32_t w[16][sizeof(T) / 2];
+};
+
+template <typename T>
+__device__ __forceinline__ void load_strip(const uint8_t *stage, int rbl, int hc, int pass, ColStrip<T> &st) {
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+        const int row = rbl * 16 + r;
+        const uint8_t *p = stage + row * 128 + ((((hc >> 1) ^ (row & 7)) << 4) | ((hc & 1) << 3));
+        if (sizeof(T) == 2) {
+            st.w[r][0] = *reinterpret_cast<const uint32_t *>(p + 4 * pass);
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2 *>(p);
+            st.w[r][0] = v.x;
+            st.w[r][sizeof(T) / 2 - 1] = v.y;
+        }
+    }
+}
+
+// Column h (0, 1) of a strip as block pairs (rows 2m, 2m+1); with FIRST the
+// butterfly's first stage applied (bf16: the even row's element enters the
+// adds as a bf16 operand, which widens exactly).
+template <typename T, bool FIRST>
+__device__ __forceinline__ void strip_column(const ColStrip<T> &st, int h, f2 (&v)[8]) {
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+        if (sizeof(T) == 2) {
+            const uint32_t a = st.w[2 * m][0], b = st.w[2 * m + 1][0];
+            if (!FIRST) {
+                v[m] = h ? f2{bf16_hi(a), bf16_hi(b)} : f2{bf16_lo(a), bf16_lo(b)};
+            } else {
+                const float fb = h ? bf16_hi(b) : bf16_lo(b);
+                if (h)
+                    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, hi, %3; sub.rn.f32.bf16 %1, hi, %3; }"
+                        : "=f"(v[m].x), "=f"(v[m].y) : "r"(a), "f"(fb));
+                else
+                    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, lo, %3; sub.rn.f32.bf16 %1, lo, %3; }"
+                        : "=f"(v[m].x), "=f"(v[m].y) : "r"(a), "f"(fb));
+            }
+        } else {
+            v[m] = f2{__uint_as_float(st.w[2 * m][h]), __uint_as_float(st.w[2 * m + 1][h])};
+        }
+    }
+    if (FIRST && sizeof(T) != 2) fwht16_first(v);
+}
+
 template <int MODE, bool RHT, typename T, bool AP>
-__global__ void __launch_bounds__(16 * kColRBT, 4) k_quant_col(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
+__global__ void __launch_bounds__(16 * kColRBT) k_quant_col(const __grid_constant__ CUtensorMap tmap, const QArgs a) {
     constexpr int RBT = kColRBT;
     using CT = ColTile<T, RBT>;
-    constexpr int TC = CT::TC, HC = CT::HC;
+    constexpr int TC = CT::TC, HC = CT::HC, PASSES = HC / 2;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ DivTable tab;
     __shared__ RhtMult rm;
     __shared__ __align__(8) uint64_t full[2];
     uint8_t *in = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
-    uint8_t *oc = in + 2 * CT::kStageBytes;
-    uint8_t *os = oc + 2 * CT::kCodeBytes;
     const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, RB = R >> 4, csp = (RB + 3) & ~3u;
     const uint32_t ntc = (C + TC - 1) / TC, ntr = (R + CT::TR - 1) / CT::TR;
     const uint32_t ntiles = ntc * ntr;
@@ -183,9 +237,6 @@ __global__ void __launch_bounds__(16 * kColRBT, 4) k_quant_col(const __grid_cons
     tensor_amax_done(a, A, g);
 
     const int64_t code_pitch = R >> 1;
-    const bool codes16 = (code_pitch & 15) == 0 && (reinterpret_cast<uintptr_t>(a.codes_col) & 15u) == 0;
-    const bool words = (reinterpret_cast<uintptr_t>(a.scales_col) & 3u) == 0;
-    const bool lin_words = words && (RB & 3u) == 0;
     for (uint32_t k = 0;; ++k) {
         const uint32_t t = blockIdx.x + k * gridDim.x;
         if (t >= ntiles) break;
@@ -194,51 +245,46 @@ __global__ void __launch_bounds__(16 * kColRBT, 4) k_quant_col(const __grid_cons
             wait_gave_up(a, a.gscale);
         }
         const uint32_t tr = t / ntc, tc = t - tr * ntc;
-        const uint32_t rb0 = tr * RBT, o0 = tc * TC, rb = rb0 + rbl;
+        const uint32_t rb = tr * RBT + rbl, o0 = tc * TC;
         const uint8_t *stage = in + s * CT::kStageBytes;
-        uint8_t *ocs = oc + s * CT::kCodeBytes;
-        uint8_t *oss = os + s * CT::kScaleBytes;
-        uint2 w[16];
 #pragma unroll
-        for (int r = 0; r < 16; r++) {
-            const int row = rbl * 16 + r;
-            w[r] = *reinterpret_cast<const uint2 *>(stage + row * 128 + ((((hc >> 1) ^ (row & 7)) << 4) |
-                                                                           ((hc & 1) << 3)));
-        }
-        uint4 rnd[HC];
+        for (int pass = 0; pass < PASSES; pass++) {
+            ColStrip<T> st;
+            load_strip<T>(stage, rbl, hc, pass, st);
+            uint4 rnd[2];
 #pragma unroll
-        for (int cc = 0; cc < HC; cc++) {
-            rnd[cc] = make_uint4(0u, 0u, 0u, 0u);
-            if (MODE == MODE_SR) {
-                const uint64_t blk = a.blk_base + (uint64_t)(o0 + HC * hc + cc) * RB + rb;
-                rnd[cc] = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
-                                              (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
-            }
-        }
-#pragma unroll
-        for (int cc = 0; cc < HC; cc++) {
-            const int ol = HC * hc + cc;
-            uint32_t S = 0;
-            uint2 c = make_uint2(0u, 0u);
-            if (rb < RB && o0 + ol < C) {
-                f2 v[8];
-                if (fast && RHT) {
-                    strip_fwht_first<T>(w, cc, v);
-                    c = encode_block_fast<MODE, RHT, AP, true>(v, sd, tab, signs, rnd[cc], S);
-                } else if (fast) {
-                    strip_block<T>(w, cc, v);
-                    c = encode_block_fast<MODE, RHT, AP>(v, sd, tab, signs, rnd[cc], S);
-                } else {
-                    strip_block<T>(w, cc, v);
-                    if (RHT) rht16(v, rm);
-                    c = encode_block<MODE>(v, sd, tab, rnd[cc], S);
+            for (int h = 0; h < 2; h++) {
+                rnd[h] = make_uint4(0u, 0u, 0u, 0u);
+                if (MODE == MODE_SR) {
+                    const uint64_t blk = a.blk_base + (uint64_t)(o0 + HC * hc + 2 * pass + h) * RB + rb;
+                    rnd[h] = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
+                                                 (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
                 }
             }
-            // slot rbl of output row ol, XOR-swizzled by ol / HC (= hc)
-            *reinterpret_cast<uint2 *>(ocs + ol * CT::kPitch + ((rbl ^ (hc & (RBT - 1))) << 3)) = c;
-            oss[rbl * TC + ol] = (uint8_t)S;
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const uint32_t o = o0 + HC * hc + 2 * pass + h;  // output row = X column
+                if (rb < RB && o < C) {
+                    uint32_t S = 0;
+                    uint2 c;
+                    f2 v[8];
+                    if (fast && RHT) {
+                        strip_column<T, true>(st, h, v);
+                        c = encode_block_fast<MODE, RHT, AP, true>(v, sd, tab, signs, rnd[h], S);
+                    } else if (fast) {
+                        strip_column<T, false>(st, h, v);
+                        c = encode_block_fast<MODE, RHT, AP>(v, sd, tab, signs, rnd[h], S);
+                    } else {
+                        strip_column<T, false>(st, h, v);
+                        if (RHT) rht16(v, rm);
+                        c = encode_block<MODE>(v, sd, tab, rnd[h], S);
+                    }
+                    *reinterpret_cast<uint2 *>(a.codes_col + (int64_t)o * code_pitch + (int64_t)rb * 8) = c;
+                    a.scales_col[a.swizzled ? swizzle_offset32(o, rb, csp) : o * RB + rb] = (uint8_t)S;
+                }
+            }
         }
-        __syncthreads();  // output tile complete, stage s consumed
+        __syncthreads();  // stage s consumed
         if (tid == 0) {
             const uint32_t tn = t + 2 * gridDim.x;
             if (tn < ntiles) {
@@ -248,7 +294,6 @@ __global__ void __launch_bounds__(16 * kColRBT, 4) k_quant_col(const __grid_cons
                             (int32_t)((tn / ntc) * CT::TR), &full[s]);
             }
         }
-        write_col_tile<T, RBT>(a, ocs, oss, o0, rb0, C, RB, csp, code_pitch, codes16, words, lin_words, tid);
     }
 }
 
@@ -456,9 +501,9 @@ __global__ void __launch_bounds__(16 * kColRBT, 5) k_quant_2d(const __grid_const
 // Persistent grid over the tiles (programmatic dependent launch: the first
 // tiles are staged while the amax pass finishes).
 template <typename CT, typename K>
-cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, cudaStream_t s) {
+cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, int smem, cudaStream_t s) {
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, CT::NT, CT::kSmemBytes);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, CT::NT, smem);
     if (per_sm < 1) per_sm = 1;
     const int64_t tiles = ((a.rows + CT::TR - 1) / CT::TR) * ((a.cols + CT::TC - 1) / CT::TC);
     const int64_t cap = (int64_t)sm_count() * per_sm;
@@ -466,7 +511,7 @@ cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, cudaStream
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(CT::NT);
-    cfg.dynamicSmemBytes = CT::kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -479,7 +524,7 @@ cudaError_t launch_tiles(K k, const CUtensorMap &map, const QArgs &a, cudaStream
 template <int MODE, bool RHT, typename T, bool AP>
 cudaError_t run_col(const QArgs &a, cudaStream_t s) {
     auto k = k_quant_col<MODE, RHT, T, AP>;
-    constexpr int smem = ColTile<T, kColRBT>::kSmemBytes;
+    constexpr int smem = 2 * ColTile<T, kColRBT>::kStageBytes + 1024;  // input stages only
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -489,7 +534,7 @@ cudaError_t run_col(const QArgs &a, cudaStream_t s) {
     CUtensorMap map;
     if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, ColTile<T, kColRBT>::TC, ColTile<T, kColRBT>::TR))
         return cudaErrorInvalidValue;
-    return launch_tiles<ColTile<T, kColRBT>>(k, map, a, s);
+    return launch_tiles<ColTile<T, kColRBT>>(k, map, a, smem, s);
 }
 
 template <typename T, bool AP>
@@ -505,7 +550,7 @@ cudaError_t run_2d(const QArgs &a, cudaStream_t s) {
     CUtensorMap map;
     if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, ColTile<T, kColRBT>::TC, ColTile<T, kColRBT>::TR))
         return cudaErrorInvalidValue;
-    return launch_tiles<ColTile<T, kColRBT>>(k, map, a, s);
+    return launch_tiles<ColTile<T, kColRBT>>(k, map, a, ColTile<T, kColRBT>::kSmemBytes, s);
 }
 
 template <typename T, bool AP>
