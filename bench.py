@@ -442,7 +442,7 @@ def kernel_plan(w: wl.Workload) -> tuple[str | None, str]:
         return None, ("k_quant_rowscaled_staged" if w.cols * 2 <= ROWSCALED_STAGED_MAX_ROW_BYTES
                       else "k_quant_rowscaled")
     if w.groups:
-        return "k_amax_groups", "k_quant_rowscaled_staged"
+        return "k_amax_groups", "k_quant_row_grouped"
     if w.amax_given:  # the quantize kernel alone (the one-kernel path needs to compute the amax)
         return None, ("k_quant_2d" if w.block2d else "k_quant_col" if not w.rowwise else "k_quant_row")
     if w.rowwise and not w.colwise and not w.block2d and w.rows * w.cols <= FUSED_MAX_ELEMS:
@@ -462,7 +462,7 @@ def call_kernels(w: wl.Workload) -> list[str]:
     if two_scales(w):  # one amax read for both orientations
         return ["k_amax_tma_cols", "k_quant_row", "k_quant_col"]
     if w.groups:
-        return ["k_amax_groups", "k_group_finalize", "k_quant_rowscaled_staged"]
+        return ["k_amax_groups", "k_group_finalize", "k_quant_row_grouped"]
     return [k for k in kernel_plan(w) if k]
 
 

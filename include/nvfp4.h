@@ -248,11 +248,13 @@ nvfp4_status nvfp4_quantize_four_over_six(const nvfp4_input *in, uint32_t flags,
  * gets 0), with the block scales and codes written into the rows of the one
  * output.  Philox blocks keep their numbers in the whole input.  mode: one of
  * NVFP4_MODE_*.  flags: NVFP4_ROWWISE (required), NVFP4_SWIZZLED,
- * NVFP4_AMAX_GIVEN (out->amax holds the n_groups amaxes).  Rows are staged in
- * shared memory: cols * element size <= 96 KiB, else NVFP4_ERR_UNSUPPORTED.
- * Needs no workspace.  Launches an amax kernel, a tiny finalising kernel and
- * the per-row-scale quantize kernel (which takes each row's scale from its
- * group). */
+ * NVFP4_AMAX_GIVEN (out->amax holds the n_groups amaxes).  Needs no
+ * workspace.  Launches an amax kernel, a tiny finalising kernel and the tiled
+ * rowwise quantize kernel, which encodes each row with its group's scale
+ * (divisor tables of two groups per CTA; rows of groups shorter than a tile
+ * compute their divisors directly, with the same result).  NVFP4_ERR_UNSUPPORTED
+ * only if the input's tensor map cannot be made and a row is longer than
+ * 96 KiB (the per-row fallback stages whole rows in shared memory). */
 enum { NVFP4_MODE_RNE = 0, NVFP4_MODE_SR = 1, NVFP4_MODE_RHT_SR = 2, NVFP4_MODE_FOUR_OVER_SIX = 3 };
 nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const int64_t *group_offsets,
                                     int64_t n_groups, int32_t mode, uint16_t sign_mask, uint64_t seed,

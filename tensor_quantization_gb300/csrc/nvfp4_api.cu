@@ -263,8 +263,6 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
     if (n_groups < 1 || n_groups > in->rows + 1 || !group_offsets) return NVFP4_ERR_INVALID_ARG;
     if (in->cols % 16 != 0 || in->col0 != 0) return NVFP4_ERR_INVALID_ARG;
     if (!out->amax || !out->global_scale) return NVFP4_ERR_INVALID_ARG;
-    const int64_t esz = elem_size(in->dtype);
-    if (in->cols * esz > 96 * 1024) return NVFP4_ERR_UNSUPPORTED;  // rows are staged in shared memory
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool given = flags & NVFP4_AMAX_GIVEN;
     const bool rht = mode == NVFP4_MODE_RHT_SR;
@@ -296,8 +294,12 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
         if (st != NVFP4_OK) return st;
     }
     st = cuda_status(nvfp4::launch_group_finalize(a, rht, given, s));
-    if (st == NVFP4_OK) st = cuda_status(nvfp4::launch_quant_rowscaled(a, fp32, kmode, rht, s));
-    if (st == NVFP4_OK && (flags & NVFP4_SWIZZLED))
+    if (st != NVFP4_OK) return st;
+    bool padded = true;
+    const cudaError_t e = nvfp4::launch_quant_grouped(a, fp32, kmode, rht, &padded, s);
+    if (e == cudaErrorNotSupported) return NVFP4_ERR_UNSUPPORTED;
+    st = cuda_status(e);
+    if (st == NVFP4_OK && !padded && (flags & NVFP4_SWIZZLED))
         st = cuda_status(nvfp4::launch_scale_pad(out->scales_row, in->rows, in->cols / 16, s));
     return st;
 }

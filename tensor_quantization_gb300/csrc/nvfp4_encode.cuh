@@ -63,6 +63,20 @@ __device__ __forceinline__ void build_table(DivTable &T, float g, int tid, int n
     }
 }
 
+// The same entries computed when they are looked up (a block whose global
+// scale has no table in shared memory); T.e[s] gives the bits of the table's
+// entry s.
+struct DivDirect {
+    struct Entries {
+        float g, up;
+        __device__ __forceinline__ Divisor operator[](uint32_t s) const {
+            Divisor D = make_divisor(__fmul_rn(e4m3_value(s), g));
+            if (up != 1.0f) D = scale_divisor(D, up, 1.0f / up);
+            return D;
+        }
+    } e;
+};
+
 // Divisors M*g of the block-scale computation (M = 6, and 4 for four-over-six).
 struct ScaleDiv {
     Divisor m6, m4;
@@ -108,9 +122,8 @@ __device__ __forceinline__ uint2 encode_codes(const f2 (&y)[8], const Divisor &D
     return c;
 }
 
-template <bool SR>
-__device__ __forceinline__ uint2 encode_with_scale(const f2 (&y)[8], uint32_t S, const DivTable &T,
-                                                   const uint4 &rnd) {
+template <bool SR, typename Tab>
+__device__ __forceinline__ uint2 encode_with_scale(const f2 (&y)[8], uint32_t S, const Tab &T, const uint4 &rnd) {
     if (S == 0u) return make_uint2(0u, 0u);
     return encode_codes<SR>(y, T.e[S & 0x7Fu], rnd);
 }
@@ -168,9 +181,9 @@ __device__ __forceinline__ float candidate_error_neg(const f2 (&y)[8], const uin
 }
 
 // Encode one block in the given mode.  Returns the codes and writes S.
-template <int MODE>
-__device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &sd, const DivTable &T,
-                                              const uint4 &rnd, uint32_t &S_out) {
+template <int MODE, typename Tab>
+__device__ __forceinline__ uint2 encode_block(const f2 (&y)[8], const ScaleDiv &sd, const Tab &T, const uint4 &rnd,
+                                              uint32_t &S_out) {
     const float am = block_amax(y);
     if (MODE == MODE_4O6) {
         const uint32_t S6 = block_scale(am, sd.m6, sd.fast6);
@@ -261,9 +274,9 @@ __device__ __forceinline__ uint2 encode_fast_vals(const f2 (&v)[8], const Diviso
 // applied here and the 0.25 / signs are folded as above; STAGE1: v already
 // holds the butterfly's first stage).  AP (fast math) replaces the exact
 // element quotient by y * RN(1/d); block scales stay exact.
-template <int MODE, bool RHT, bool AP = false, bool STAGE1 = false, bool PRE = false>
-__device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &sd, const DivTable &T,
-                                                   uint2 signs, const uint4 &rnd, uint32_t &S_out) {
+template <int MODE, bool RHT, bool AP = false, bool STAGE1 = false, bool PRE = false, typename Tab = DivTable>
+__device__ __forceinline__ uint2 encode_block_fast(f2 (&v)[8], const ScaleDiv &sd, const Tab &T, uint2 signs,
+                                                   const uint4 &rnd, uint32_t &S_out) {
     if (RHT && !STAGE1) fwht16_first(v);
     if (RHT) fwht16_rest(v);
     float am = block_amax(v);

@@ -83,6 +83,11 @@ cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht
 // caller has zeroed), then amax[g] / global_scale[g] finalised in place.
 cudaError_t launch_amax_groups(const QArgs &a, bool fp32, bool rht, cudaStream_t s);
 cudaError_t launch_group_finalize(const QArgs &a, bool rht, bool given, cudaStream_t s);
+// Grouped rowwise quantize (after the finalising kernel): each row encoded with
+// its group's global scale.  *padded: the launch also wrote the pad bytes of a
+// swizzled scale layout (false only on the fallback for inputs the tile kernel
+// cannot map; cudaErrorNotSupported when neither applies).
+cudaError_t launch_quant_grouped(const QArgs &a, bool fp32, int mode, bool rht, bool *padded, cudaStream_t s);
 // Per-tensor rowwise quantize including the amax pass, one cooperative launch
 // (an error return means nothing was enqueued).
 cudaError_t launch_quant_row_fused(const QArgs &a, bool fp32, int mode, bool rht, cudaStream_t s);

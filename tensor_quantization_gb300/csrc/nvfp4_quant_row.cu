@@ -19,4 +19,9 @@ cudaError_t launch_quant_rowscaled(const QArgs &a, bool fp32, int mode, bool rht
                        : quant_row_launch<false>(a, fp32, mode, rht, true, s);
 }
 
+cudaError_t launch_quant_grouped(const QArgs &a, bool fp32, int mode, bool rht, bool *padded, cudaStream_t s) {
+    return fp32 ? dispatch_row_grouped<float>(a, mode, rht, padded, s)
+                : dispatch_row_grouped<bf16_t>(a, mode, rht, padded, s);
+}
+
 }  // namespace nvfp4

@@ -48,8 +48,8 @@ __device__ __forceinline__ void store_scale(const QArgs &a, uint8_t *scales, uin
 
 // Encode one block from its raw bytes (flat block index i, for the Philox
 // counter); returns the codes and writes S.
-template <int MODE, bool RHT, typename T>
-__device__ __forceinline__ uint2 row_block(const QArgs &a, const ScaleDiv &sd, const DivTable &tab, const RhtMult &rm,
+template <int MODE, bool RHT, typename T, typename Tab>
+__device__ __forceinline__ uint2 row_block(const QArgs &a, const ScaleDiv &sd, const Tab &tab, const RhtMult &rm,
                                            const RawBlock<T> &raw, uint32_t i, uint32_t &S) {
     f2 v[8];
     unpack(raw, v);
@@ -106,6 +106,105 @@ __device__ __forceinline__ void issue_tile(const CUtensorMap *map, uint8_t *stag
     for (int b = 0; b < RowTile<T>::kBoxes; b++)
         tma_load_2d(stage + b * RowTile<T>::kBoxBytes, map, (int32_t)(tc * kTileCols + b * RowTile<T>::kBoxCols),
                     (int32_t)(tr * kTileRows), bar);
+}
+
+// Group of row r among groups lo..hi: the largest g <= hi with
+// group_offsets[g] <= r, else lo (binary search).
+__device__ __forceinline__ int64_t group_in(const QArgs &a, int64_t r, int64_t lo, int64_t hi) {
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.group_offsets + mid) <= r) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int64_t group_of(const QArgs &a, int64_t r) { return group_in(a, r, 0, a.n_groups - 1); }
+
+// One thread's tile row: its four blocks (j0 .. j0 + 3 of row `row`, staged
+// in `stage` as tile row `trow`) encoded with the divisor table `tab` of one
+// global scale, then their codes (32 contiguous bytes) and scales (one word)
+// stored.  fast: every divisor of that scale is in the fast range (the table
+// then carries FastScale::up).
+template <int MODE, bool RHT, typename T, bool AP, typename Tab>
+__device__ __forceinline__ void encode_tile_row(const QArgs &a, const uint8_t *stage, int trow, uint32_t row,
+                                                uint32_t j0, uint32_t C, uint32_t CS, uint32_t csp, const Tab &tab,
+                                                const ScaleDiv &sd, const RhtMult &rm, uint2 signs, bool fast,
+                                                bool codes16, bool words, bool lin_words) {
+    uint32_t S[4] = {0u, 0u, 0u, 0u};
+    uint2 c[4];
+    if (fast) {
+        // the four blocks' random words first: independent integer work
+        // the scheduler can interleave with the butterflies and divisions
+        uint4 rnd[4];
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            rnd[b] = make_uint4(0u, 0u, 0u, 0u);
+            if (MODE == MODE_SR) {
+                const uint64_t blk = a.blk_base + (uint64_t)(row * CS + j0 + b);
+                rnd[b] = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
+                                             (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
+            }
+        }
+        // (encoding the zero-filled blocks past the last column instead of
+        // branching around them measured 1 us slower per 8192x4096 call)
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            if (j0 + b < CS) {
+                RawBlock<T> raw;
+                stage_block<T>(stage, trow, b, raw);
+                f2 v[8];
+                if (RHT) unpack_fwht_first(raw, v);
+                else unpack(raw, v);
+                c[b] = encode_block_fast<MODE, RHT, AP, true, true>(v, sd, tab, signs, rnd[b], S[b]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            if (j0 + b < CS) {
+                RawBlock<T> raw;
+                stage_block<T>(stage, trow, b, raw);
+                c[b] = row_block<MODE, RHT, T>(a, sd, tab, rm, raw, row * CS + j0 + b, S[b]);
+            }
+        }
+    }
+    uint8_t *codes = a.codes_row + (int64_t)row * (C >> 1) + j0 * 8;
+    if (codes16 && j0 + 3 < CS) {
+        reinterpret_cast<uint4 *>(codes)[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+        reinterpret_cast<uint4 *>(codes)[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+            if (j0 + b < CS) reinterpret_cast<uint2 *>(codes)[b] = c[b];
+    }
+    const uint32_t word = S[0] | (S[1] << 8) | (S[2] << 16) | (S[3] << 24);
+    if (a.swizzled) {
+        uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+        if (words) {
+            *reinterpret_cast<uint32_t *>(dst) = word;
+        } else {
+#pragma unroll
+            for (int b = 0; b < 4; b++) dst[b] = (uint8_t)S[b];
+        }
+    } else if (lin_words && j0 + 3 < CS) {
+        *reinterpret_cast<uint32_t *>(a.scales_row + row * CS + j0) = word;
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+            if (j0 + b < CS) a.scales_row[row * CS + j0 + b] = (uint8_t)S[b];
+    }
+}
+
+// Zero scale word of a pad row of the swizzled layout (rows R .. Rp - 1).
+__device__ __forceinline__ void pad_tile_row(const QArgs &a, uint32_t row, uint32_t j0, uint32_t csp, bool words) {
+    uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
+    if (words) {
+        *reinterpret_cast<uint32_t *>(dst) = 0u;
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; b++) dst[b] = 0;
+    }
 }
 
 template <int MODE, bool RHT, typename T, bool AP>
@@ -171,77 +270,10 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
         const uint32_t row = tr * kTileRows + tid, j0 = tc * 4;
         const uint8_t *stage = stages + s * RowTile<T>::kStageBytes;
         if (row < R) {
-            uint32_t S[4] = {0u, 0u, 0u, 0u};
-            uint2 c[4];
-            if (fast) {
-                // the four blocks' random words first: independent integer work
-                // the scheduler can interleave with the butterflies and divisions
-                uint4 rnd[4];
-#pragma unroll
-                for (int b = 0; b < 4; b++) {
-                    rnd[b] = make_uint4(0u, 0u, 0u, 0u);
-                    if (MODE == MODE_SR) {
-                        const uint64_t blk = a.blk_base + (uint64_t)(row * CS + j0 + b);
-                        rnd[b] = philox4x32_10_keyed((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)a.offset,
-                                                     (uint32_t)(a.offset >> 32), a.round_key0, a.round_key1);
-                    }
-                }
-                // (encoding the zero-filled blocks past the last column instead of
-                // branching around them measured 1 us slower per 8192x4096 call)
-#pragma unroll
-                for (int b = 0; b < 4; b++) {
-                    if (j0 + b < CS) {
-                        RawBlock<T> raw;
-                        stage_block<T>(stage, tid, b, raw);
-                        f2 v[8];
-                        if (RHT) unpack_fwht_first(raw, v);
-                        else unpack(raw, v);
-                        c[b] = encode_block_fast<MODE, RHT, AP, true, true>(v, sd, tab, signs, rnd[b], S[b]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; b++) {
-                    if (j0 + b < CS) {
-                        RawBlock<T> raw;
-                        stage_block<T>(stage, tid, b, raw);
-                        c[b] = row_block<MODE, RHT, T>(a, sd, tab, rm, raw, row * CS + j0 + b, S[b]);
-                    }
-                }
-            }
-            uint8_t *codes = a.codes_row + (int64_t)row * (C >> 1) + j0 * 8;
-            if (codes16 && j0 + 3 < CS) {
-                reinterpret_cast<uint4 *>(codes)[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
-                reinterpret_cast<uint4 *>(codes)[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; b++)
-                    if (j0 + b < CS) reinterpret_cast<uint2 *>(codes)[b] = c[b];
-            }
-            const uint32_t word = S[0] | (S[1] << 8) | (S[2] << 16) | (S[3] << 24);
-            if (a.swizzled) {
-                uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
-                if (words) {
-                    *reinterpret_cast<uint32_t *>(dst) = word;
-                } else {
-#pragma unroll
-                    for (int b = 0; b < 4; b++) dst[b] = (uint8_t)S[b];
-                }
-            } else if (lin_words && j0 + 3 < CS) {
-                *reinterpret_cast<uint32_t *>(a.scales_row + row * CS + j0) = word;
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; b++)
-                    if (j0 + b < CS) a.scales_row[row * CS + j0 + b] = (uint8_t)S[b];
-            }
+            encode_tile_row<MODE, RHT, T, AP>(a, stage, tid, row, j0, C, CS, csp, tab, sd, rm, signs, fast, codes16,
+                                              words, lin_words);
         } else if (a.swizzled && row < Rp) {  // pad rows of the swizzled layout
-            uint8_t *dst = a.scales_row + swizzle_offset32(row, j0, csp);
-            if (words) {
-                *reinterpret_cast<uint32_t *>(dst) = 0u;
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; b++) dst[b] = 0;
-            }
+            pad_tile_row(a, row, j0, csp, words);
         }
         advance(tr, tc);
         __syncthreads();  // every thread is done with stage s
@@ -250,6 +282,119 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
             issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], ir, ic);
         }
         advance(ir, ic);
+    }
+}
+
+// ---------------------------------------------------------------------
+// Grouped rowwise quantize on the tiles of k_quant_row.
+//
+// Row groups [offs[g], offs[g+1]) each have their own global scale, written
+// by the finalising kernel before this one reads it.  Tiles are mostly inside
+// one group, or across the boundary of two: the CTA holds the divisor tables
+// of two groups in shared memory (a two-entry cache that keeps a tile's first
+// and last group), so a tile costs a table build only when it needs a group
+// the cache does not hold.  Rows of the groups strictly inside a tile (groups
+// shorter than a tile) look each divisor up through DivDirect instead, with
+// the same bits.  The tiles cover every byte of the swizzled scale layout,
+// pad rows and columns included.
+template <int MODE, bool RHT, typename T>
+__global__ void __launch_bounds__(kTileRows) k_quant_row_grouped(const __grid_constant__ CUtensorMap tmap,
+                                                                 const QArgs a) {
+    struct Slot {
+        DivTable t;
+        ScaleDiv sd;
+        int fast;
+    };
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ Slot slot[2];
+    __shared__ RhtMult rm;
+    __shared__ __align__(8) uint64_t full;
+    uint8_t *stage = dyn_smem + ((1024u - (smem_addr(dyn_smem) & 1023u)) & 1023u);
+    const uint32_t R = (uint32_t)a.rows, C = (uint32_t)a.cols, CS = C >> 4, csp = (CS + 3) & ~3u;
+    const uint32_t Rp = (R + 127) & ~127u;
+    const uint32_t ntc = (C + kTileCols - 1) / kTileCols, ntr = (R + kTileRows - 1) / kTileRows;
+    const uint32_t ntiles = ntc * ntr;
+    const int tid = threadIdx.x;
+    const uint32_t G = gridDim.x, dr = G / ntc, dc = G - dr * ntc;
+    uint32_t tr = blockIdx.x / ntc, tc = blockIdx.x - tr * ntc;
+    if (tid == 0) {
+        mbar_init(&full, 1);
+        mbar_init_fence();
+        if (blockIdx.x < ntiles) issue_tile<T>(&tmap, stage, &full, tr, tc);
+    }
+    const uint2 signs = RHT ? rht_sign_words(a.sign_mask) : make_uint2(0u, 0u);
+    if (RHT) build_rht_mult(rm, a.sign_mask, tid);
+    grid_dependency_wait();  // the group scales are final from here on
+    __syncthreads();
+    const bool codes16 = (C & 31u) == 0 && (reinterpret_cast<uintptr_t>(a.codes_row) & 15u) == 0;
+    const bool words = (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
+    const bool lin_words = words && (CS & 3u) == 0;
+    constexpr float up = FastScale<MODE, RHT>::up;
+    int64_t held0 = -1, held1 = -1;  // the groups whose tables the slots hold (uniform)
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t t = blockIdx.x + k * G;
+        if (t >= ntiles) break;
+        const uint32_t r0 = tr * kTileRows, row = r0 + tid, j0 = tc * 4;
+        const int64_t glo = group_in(a, r0, 0, a.n_groups - 1);
+        const int64_t ghi = group_in(a, min(R, r0 + kTileRows) - 1, glo, a.n_groups - 1);
+        // slots for the tile's first and last group, keeping what is held
+        int64_t n0 = held0, n1 = held1;
+        if (n0 != glo && n1 != glo) {
+            if (n0 == ghi) n1 = glo;
+            else n0 = glo;
+        }
+        if (ghi != glo && n0 != ghi && n1 != ghi) {
+            if (n0 == glo) n1 = ghi;
+            else n0 = ghi;
+        }
+        if (n0 != held0 || n1 != held1) {  // the previous tile's barrier freed the slots
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
+                const int64_t gq = q ? n1 : n0;
+                if (gq == (q ? held1 : held0)) continue;
+                const float g = a.gscale[gq];
+                const bool fast = scale_all_fast(g);
+                build_table(slot[q].t, g, tid, kTileRows, fast ? up : 1.0f);
+                if (tid == 0) {
+                    slot[q].sd = make_scale_div(g);
+                    slot[q].fast = fast;
+                }
+            }
+            held0 = n0;
+            held1 = n1;
+            __syncthreads();
+        }
+        const int64_t mine = row < R ? group_in(a, row, glo, ghi) : -1;
+        if (!mbar_wait(&full, k & 1u)) {  // a copy never landed: bounded, visible failure
+            wait_gave_up(a, nullptr);
+            if (row < R) *reinterpret_cast<volatile float *>(a.gscale + mine) = __uint_as_float(0x7FFFFFFFu);
+        }
+        if (row < R) {
+            if (mine == held0 || mine == held1) {
+                const Slot &sl = slot[mine == held0 ? 0 : 1];
+                encode_tile_row<MODE, RHT, T, false>(a, stage, tid, row, j0, C, CS, csp, sl.t, sl.sd, rm, signs,
+                                                     sl.fast != 0, codes16, words, lin_words);
+            } else {
+                const float g = a.gscale[mine];
+                const bool fast = scale_all_fast(g);
+                const DivDirect dd{{g, fast ? up : 1.0f}};
+                encode_tile_row<MODE, RHT, T, false>(a, stage, tid, row, j0, C, CS, csp, dd, make_scale_div(g), rm,
+                                                     signs, fast, codes16, words, lin_words);
+            }
+        } else if (a.swizzled && row < Rp) {
+            pad_tile_row(a, row, j0, csp, words);
+        }
+        tc += dc;
+        tr += dr;
+        if (tc >= ntc) {
+            tc -= ntc;
+            ++tr;
+        }
+        __syncthreads();  // every thread is done with the stage and the slots
+        if (tid == 0 && t + G < ntiles) {
+            fence_async_shared();
+            issue_tile<T>(&tmap, stage, &full, tr, tc);
+        }
     }
 }
 
@@ -531,17 +676,6 @@ struct RowTables {
     Divisor m6, m4;
 };
 
-// Group of row r: the largest g with group_offsets[g] <= r (binary search).
-__device__ __forceinline__ int64_t group_of(const QArgs &a, int64_t r) {
-    int64_t lo = 0, hi = a.n_groups - 1;
-    while (lo < hi) {
-        const int64_t mid = (lo + hi + 1) >> 1;
-        if (__ldg(a.group_offsets + mid) <= r) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
 template <typename T>
 __device__ __forceinline__ void smem_row_block(const uint8_t *rowp, uint32_t j, RawBlock<T> &b) {
     const uint4 *p = reinterpret_cast<const uint4 *>(rowp + (size_t)j * 16 * sizeof(T));
@@ -768,9 +902,6 @@ cudaError_t run_rowscaled_staged(const QArgs &a, cudaStream_t s) {
 template <int MODE, bool RHT, typename T, bool AP>
 cudaError_t run_rowscaled(const QArgs &a, cudaStream_t s) {
     if ((uint64_t)a.cols * sizeof(T) <= kMaxStagedRowBytes) {
-        if constexpr (!AP) {  // row groups (always exact quotients)
-            if (a.n_groups > 0) return run_rowscaled_staged<MODE, RHT, T, false, true>(a, s);
-        }
         return run_rowscaled_staged<MODE, RHT, T, AP, false>(a, s);
     }
     auto k = k_quant_rowscaled<MODE, RHT, T>;
@@ -794,6 +925,54 @@ cudaError_t dispatch_row(const QArgs &a, int mode, bool rht, bool scaled_rows, c
     if (mode == MODE_SR) return rht ? run_row<MODE_SR, true, T, AP>(a, s) : run_row<MODE_SR, false, T, AP>(a, s);
     if constexpr (!AP) return run_row<MODE_4O6, false, T, false>(a, s);
     return cudaErrorInvalidValue;
+}
+
+// Grouped rowwise quantize: the tile kernel, launched while the finalising
+// kernel runs (it waits for it before reading the group scales).  If the
+// tensor map cannot be made, rows that fit in shared memory take the staged
+// per-row kernel instead (*padded = false: the caller zeroes the pad bytes of
+// the swizzled layout, which that kernel leaves alone).
+template <int MODE, bool RHT, typename T>
+cudaError_t run_row_grouped(const QArgs &a, bool *padded, cudaStream_t s) {
+    auto k = k_quant_row_grouped<MODE, RHT, T>;
+    constexpr int smem = RowTile<T>::kStageBytes + 1024;
+    static bool configured = false;  // one attribute call per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    CUtensorMap map;
+    if (!make_tmap_2d(&map, a.x, (int)sizeof(T), a.rows, a.cols, a.ld, RowTile<T>::kBoxCols, kTileRows)) {
+        *padded = false;
+        if ((uint64_t)a.cols * sizeof(T) > kMaxStagedRowBytes) return cudaErrorNotSupported;
+        return run_rowscaled_staged<MODE, RHT, T, false, true>(a, s);
+    }
+    *padded = true;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTileRows, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t tiles = ((a.rows + kTileRows - 1) / kTileRows) * ((a.cols + kTileCols - 1) / kTileCols);
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles < cap ? tiles : cap));
+    cfg.blockDim = dim3(kTileRows);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, map, a);
+}
+
+template <typename T>
+cudaError_t dispatch_row_grouped(const QArgs &a, int mode, bool rht, bool *padded, cudaStream_t s) {
+    if (mode == MODE_RNE) return run_row_grouped<MODE_RNE, false, T>(a, padded, s);
+    if (mode == MODE_SR) return rht ? run_row_grouped<MODE_SR, true, T>(a, padded, s)
+                                    : run_row_grouped<MODE_SR, false, T>(a, padded, s);
+    return run_row_grouped<MODE_4O6, false, T>(a, padded, s);
 }
 
 template <int MODE, bool RHT, typename T, bool AP>

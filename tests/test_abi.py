@@ -95,8 +95,10 @@ def test_arguments_are_rejected_before_any_launch(lib):
         nvfp4.ERR_UNSUPPORTED  # columnwise
     assert grp(ctypes.byref(_inp(16, 32, 32)), 1 | nvfp4.FAST_MATH, offs, 2, 0, 0, 0, 0, ctypes.byref(out),
                None) == nvfp4.ERR_UNSUPPORTED
-    assert grp(ctypes.byref(_inp(2, 65536, 65536)), 1, offs, 2, 0, 0, 0, 0, ctypes.byref(out), None) == \
-        nvfp4.ERR_UNSUPPORTED  # a 128 KiB row does not fit the row buffer
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 1, offs, 18, 0, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_INVALID_ARG  # more groups than rows + 1
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 1, None, 2, 0, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_INVALID_ARG  # no offsets
     dq = lib.nvfp4_dequantize
     assert dq(16, 16, 16, 4, 24, 0, 16, 0, None) == nvfp4.ERR_INVALID_ARG  # cols % 16
     assert dq(16, 16, 16, 4, 32, 0, 16, 9, None) == nvfp4.ERR_INVALID_ARG  # dtype

@@ -38,7 +38,7 @@ def test_counted_bytes(name, total):
     ("rowscaled_4o6_8192x8192", ["k_quant_rowscaled_staged"]),
     ("act_rht_sr_given_8192x4096", ["k_quant_row"]),
     ("act_rht_sr_rowcol_8192x4096", ["k_amax_tma_cols", "k_quant_row", "k_quant_col"]),
-    ("act_rht_sr_groups_8192x4096", ["k_amax_groups", "k_group_finalize", "k_quant_rowscaled_staged"]),
+    ("act_rht_sr_groups_8192x4096", ["k_amax_groups", "k_group_finalize", "k_quant_row_grouped"]),
 ])
 def test_call_kernels(name, kernels):
     w = wl.WORKLOADS[name]

@@ -683,6 +683,43 @@ def test_grouped_rows_each_with_its_own_scale(mode, swizzled):
     assert same_float_bits(q2.global_scale.cpu().numpy(), gscales2)
 
 
+GROUP_CASES = {
+    # rows, cols, dtype, group offsets, mode, strided
+    "fibonacci_groups": (520, 272, torch.bfloat16, [0, 1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 520],
+                         "rht_sr", False),
+    "one_row_groups": (200, 128, torch.bfloat16, list(range(201)), "sr", False),
+    "fp32_strided": (300, 240, torch.float32, [0, 129, 129, 130, 300], "4o6", True),
+    "tile_aligned": (512, 512, torch.bfloat16, [0, 128, 256, 256, 512], "rne", False),
+    "long_rows": (40, 53248, torch.bfloat16, [0, 7, 7, 40], "rht_sr", False),
+}
+
+
+@pytest.mark.parametrize("case", list(GROUP_CASES))
+def test_grouped_tiles(case):
+    """Group layouts against the tiles of the grouped kernel: many groups inside
+    one tile (their rows look divisors up without a table), a group per row,
+    fp32 rows with a pitch, boundaries on tile edges, and rows longer than
+    96 KiB; ragged column tiles and pad rows in the swizzled layout."""
+    R, C, dtype, offs, mode, strided = GROUP_CASES[case]
+    x = mixed_input(R, C, seed=31 + list(GROUP_CASES).index(case), dtype=dtype)
+    x[offs[1]:offs[2]] *= 1e-2  # a group with a scale of its own
+    if strided:
+        base = torch.zeros(R, C + 32, dtype=dtype, device="cuda")
+        base[:, 16:16 + C] = x.cuda()
+        x_dev = base[:, 16:16 + C]
+    else:
+        x_dev = to_device(x)
+    kw = dict(mode=mode, swizzled=True, sign_mask=0x1DB7, seed=15, offset=6)
+    offs_d = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    q = nvfp4.quantize_grouped(x_dev, offs_d, **kw)
+    torch.cuda.synchronize()
+    codes, scales, amaxes, gscales = _oracle_grouped(x, offs, **kw)
+    assert np.array_equal(q.codes_row.cpu().numpy(), codes)
+    assert np.array_equal(q.scales_row.cpu().numpy(), scales)
+    assert same_float_bits(q.amax.cpu().numpy(), amaxes)
+    assert same_float_bits(q.global_scale.cpu().numpy(), gscales)
+
+
 def test_grouped_one_group_is_the_per_tensor_result():
     x = mixed_input(256, 512, seed=28)
     offs_d = torch.tensor([0, 256], dtype=torch.int64, device="cuda")
