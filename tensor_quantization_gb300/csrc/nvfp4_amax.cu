@@ -419,19 +419,27 @@ __global__ void __launch_bounds__(256) k_amax_rows(const QArgs a) {
     }
 }
 
-// Grouped rowwise scaling: n_groups row ranges, each its own tensor for the
-// amax.  A CTA takes a contiguous range of rows and, for each group segment in
-// it, reduces the segment's blocks (post-RHT magnitudes without the 0.25) and
-// folds the result into amax[g] with one atomicMax on its bits (the caller
-// zeroed amax[]; magnitude bits order like the floats, NaN above +inf).
+// Per-group amax (grouped quantize): amax[g] = max over the blocks of group g,
+// as if each group were a tensor of its own.  A CTA takes a contiguous range
+// of rows and, for each group segment in it, reduces the segment's blocks
+// (post-RHT magnitudes without the 0.25) and folds the result into amax[g]
+// with one atomicMax on its bits (the caller zeroed amax[]; magnitude bits
+// order like the floats, NaN above +inf).  Block i of a segment is row
+// s0 + i / CS, column i % CS: each thread keeps a (row, column) cursor that
+// advances by the CTA's thread count without a division, and has kLdgBlocks
+// blocks in flight.  With the RHT, a block whose butterfly bound is not above
+// the warp's running maximum of the segment skips the butterfly (the skip
+// test of k_amax_ldg_rht; the maximum restarts at 0 for every segment).
 template <bool RHT, typename T>
-__global__ void __launch_bounds__(256) k_amax_groups(const QArgs a) {
+__global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_groups(const QArgs a) {
+    constexpr bool SKIP = RHT && kAmaxSkip;
     __shared__ uint32_t red[32];
     const uint32_t CS = (uint32_t)(a.cols >> 4);
     const T *x = static_cast<const T *>(a.x);
     const int64_t per = (a.rows + gridDim.x - 1) / gridDim.x;
     const int64_t r0 = (int64_t)blockIdx.x * per, r1 = min(a.rows, r0 + per);
     if (r0 >= r1) return;
+    const uint32_t nt = blockDim.x, dr = nt / CS, dj = nt - dr * CS, lane = threadIdx.x & 31;
     // the group of r0: largest g with offsets[g] <= r0
     int64_t lo = 0, hi = a.n_groups - 1;
     while (lo < hi) {
@@ -444,15 +452,47 @@ __global__ void __launch_bounds__(256) k_amax_groups(const QArgs a) {
         const int64_t s0 = max(r0, __ldg(a.group_offsets + g)), s1 = min(r1, __ldg(a.group_offsets + g + 1));
         if (s0 >= r1) break;
         if (s0 >= s1) continue;  // an empty group, or one that ends before this range
-        const uint64_t nb = (uint64_t)(s1 - s0) * CS;
+        const uint32_t nb = (uint32_t)(s1 - s0) * CS;  // < 2^30: the input has < 2^34 elements
+        const T *p = x + (s0 + threadIdx.x / CS) * a.ld + 16 * (threadIdx.x % CS);
+        uint32_t j = threadIdx.x % CS;
+        const int64_t dp = (int64_t)dr * a.ld + 16 * (int64_t)dj, back = 16 * (int64_t)CS - a.ld;
+        auto step = [&]() {  // p, j: to the block nt further on
+            p += dp;
+            j += dj;
+            if (j >= CS) {
+                j -= CS;
+                p -= back;  // one row down, CS blocks back
+            }
+        };
         uint32_t m = 0;
-        for (uint64_t i = threadIdx.x; i < nb; i += blockDim.x) {
-            const int64_t r = s0 + (int64_t)(i / CS);
-            const uint32_t j = (uint32_t)(i % CS);
-            f2 v[8];
-            load_block_row(x + r * a.ld + 16 * j, v);
-            if (RHT) fwht16(v);
-            m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+        auto reduce = [&](const RawBlock<T> &raw) {
+            if (!RHT) {
+                m = max(m, block_max_bits(raw));
+            } else if (!SKIP || butterfly_bound(raw) > m) {
+                f2 v[8];
+                unpack(raw, v);
+                fwht16(v);
+                m = max(m, __float_as_uint(block_amax(v)) & 0x7FFFFFFFu);
+            }
+        };
+        uint32_t i = threadIdx.x;
+        // full rounds: the warp's last lane still has kLdgBlocks blocks
+        for (; i - lane + 31 + (kLdgBlocks - 1) * nt < nb; i += kLdgBlocks * nt) {
+            RawBlock<T> raw[kLdgBlocks];
+#pragma unroll
+            for (int u = 0; u < kLdgBlocks; u++) {
+                load_raw(p, raw[u]);
+                step();
+            }
+#pragma unroll
+            for (int u = 0; u < kLdgBlocks; u++) reduce(raw[u]);
+            if (SKIP) m = __reduce_max_sync(0xFFFFFFFFu, m);
+        }
+        for (; i < nb; i += nt) {
+            RawBlock<T> raw;
+            load_raw(p, raw);
+            step();
+            reduce(raw);
         }
         m = block_max_u32(m, red);
         if (threadIdx.x == 0) atomicMax(bits + g, m);
@@ -587,9 +627,11 @@ template <bool RHT, typename T>
 static cudaError_t run_amax_groups(const QArgs &a, cudaStream_t s) {
     auto k = k_amax_groups<RHT, T>;
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0);
-    const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
-    k<<<(int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap), 256, 0, s>>>(a);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAmaxLdgThreads, 0);
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 4) per_sm = 4;  // as k_amax_ldg_rht: more blocks per thread
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    k<<<(int)(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap), kAmaxLdgThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -121,3 +121,19 @@ def test_both_orientations_codes_from_the_one_read_pass():
         assert np.array_equal(codes.cpu().numpy(), o["codes"])
         assert np.array_equal(scales.cpu().numpy().ravel(), o["scales"].ravel())
         assert same_bits(q.global_scale.cpu()[int(col)], o["global_scale"])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("case", CASES)
+def test_grouped_rht_amax_is_exact_with_the_skip(case, dtype):
+    """The grouped amax pass restarts its running maximum for every group
+    segment; each group's maximum must still be the oracle's, bit for bit."""
+    x = make(case, dtype)
+    offs = [0, 700, 701, 701, 1500, 2047, R]
+    xb = np_bits(x)
+    q = nvfp4.quantize_grouped(x.cuda(), torch.tensor(offs, dtype=torch.int64, device="cuda"), mode="rht_sr",
+                               sign_mask=0x5A5A, seed=3)
+    torch.cuda.synchronize()
+    want = [oracle.amax(xb[o0:o1], rht=True)[0] if o1 > o0 else np.float32([0.0])
+            for o0, o1 in zip(offs[:-1], offs[1:])]
+    assert same_bits(q.amax.cpu(), np.concatenate([np.asarray(w, np.float32).ravel() for w in want]))
