@@ -125,11 +125,17 @@ def profile_traffic(kernel: str, workload: str) -> float | None:
     return profile_field(kernel, workload, "traffic_bytes_per_launch")
 
 
+# Host-only entry-point files (argument checks and the choice of launches):
+# no kernel code or launch configuration, so not part of the kernel digest.
+HOST_ONLY_SOURCES = ("nvfp4_api.cu", "nvfp4_static.cu")
+
+
 def source_digest() -> str:
+    """Digest of the kernel sources (device code and its launchers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_quantization_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name not in HOST_ONLY_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

@@ -242,11 +242,12 @@ nvfp4_status nvfp4_quantize_four_over_six(const nvfp4_input *in, uint32_t flags,
  * four-over-six quantize #4852", PR description: grouped / MoE quantization is
  * the named follow-up).  group_offsets is a DEVICE array of n_groups+1
  * non-decreasing row indices, group_offsets[0] = 0 and group_offsets[n_groups]
- * = rows; group g is rows [group_offsets[g], group_offsets[g+1]) (it may be
+ * = rows (1 <= n_groups < 2^31; empty groups allowed, so n_groups may exceed
+ * rows); group g is rows [group_offsets[g], group_offsets[g+1]) (it may be
  * empty) and is quantized as a tensor of its own: its own amax and global
  * scale (out->amax and out->global_scale hold n_groups floats; an empty group
- * gets 0), with the block scales and codes written into the rows of the one
- * output.  Philox blocks keep their numbers in the whole input.  mode: one of
+ * gets amax 0, or the amax given with NVFP4_AMAX_GIVEN, and scale amax / 2688),
+ * with the block scales and codes written into the rows of the one output.  Philox blocks keep their numbers in the whole input.  mode: one of
  * NVFP4_MODE_*.  flags: NVFP4_ROWWISE (required), NVFP4_SWIZZLED,
  * NVFP4_AMAX_GIVEN (out->amax holds the n_groups amaxes).  Needs no
  * workspace.  Launches an amax kernel, a tiny finalising kernel and the tiled

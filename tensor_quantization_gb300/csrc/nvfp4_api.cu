@@ -260,20 +260,22 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
     if (!(flags & NVFP4_ROWWISE)) return NVFP4_ERR_INVALID_ARG;
     if (flags & (NVFP4_COLWISE | NVFP4_BLOCK_2D | NVFP4_SCALE_PER_ROW | NVFP4_FAST_MATH)) return NVFP4_ERR_UNSUPPORTED;
     if (mode < NVFP4_MODE_RNE || mode > NVFP4_MODE_FOUR_OVER_SIX) return NVFP4_ERR_INVALID_ARG;
-    if (n_groups < 1 || n_groups > in->rows + 1 || !group_offsets) return NVFP4_ERR_INVALID_ARG;
+    // groups may be empty, so there can be more groups than rows (experts without tokens)
+    if (n_groups < 1 || n_groups >= kMaxDim || !group_offsets) return NVFP4_ERR_INVALID_ARG;
     if (in->cols % 16 != 0 || in->col0 != 0) return NVFP4_ERR_INVALID_ARG;
     if (!out->amax || !out->global_scale) return NVFP4_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool given = flags & NVFP4_AMAX_GIVEN;
     const bool rht = mode == NVFP4_MODE_RHT_SR;
-    if (in->rows == 0 || in->cols == 0) {
+    nvfp4::QArgs a = make_args(in, out, nullptr, flags);
+    a.group_offsets = group_offsets;
+    a.n_groups = n_groups;
+    if (in->rows == 0 || in->cols == 0) {  // every group empty: amax 0 (or as given), g = amax / 2688
         if (!given && cudaMemsetAsync(out->amax, 0, n_groups * sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
-        return cudaMemsetAsync(out->global_scale, 0, n_groups * sizeof(float), s) == cudaSuccess ? NVFP4_OK
-                                                                                                : NVFP4_ERR_CUDA;
+        return cuda_status(nvfp4::launch_group_finalize(a, false, given, s));
     }
     if (!out->codes_row || !out->scales_row || !aligned(out->codes_row, 8)) return NVFP4_ERR_INVALID_ARG;
 
-    nvfp4::QArgs a = make_args(in, out, nullptr, flags);
     a.sign_mask = sign_mask;
     a.seed = seed;
     a.offset = offset;
@@ -282,8 +284,6 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
         a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
     }
     a.blk_base = (uint64_t)in->row0 * (uint64_t)(in->cols / 16);
-    a.group_offsets = group_offsets;
-    a.n_groups = n_groups;
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
     const int kmode = mode == NVFP4_MODE_RNE ? nvfp4::MODE_RNE_ID
                       : mode == NVFP4_MODE_FOUR_OVER_SIX ? nvfp4::MODE_4O6_ID

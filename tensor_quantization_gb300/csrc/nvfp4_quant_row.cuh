@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row_grouped(const __grid_co
     const bool words = (reinterpret_cast<uintptr_t>(a.scales_row) & 3u) == 0;
     const bool lin_words = words && (CS & 3u) == 0;
     constexpr float up = FastScale<MODE, RHT>::up;
-    const uint32_t ng = (uint32_t)a.n_groups;  // <= rows + 1 < 2^31
+    const uint32_t ng = (uint32_t)a.n_groups;  // < 2^31
     uint32_t held0 = ~0u, held1 = ~0u;  // the groups whose tables the slots hold (uniform)
     auto build = [&](int q, uint32_t gq) {
         const float g = a.gscale[gq];

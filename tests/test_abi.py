@@ -95,8 +95,8 @@ def test_arguments_are_rejected_before_any_launch(lib):
         nvfp4.ERR_UNSUPPORTED  # columnwise
     assert grp(ctypes.byref(_inp(16, 32, 32)), 1 | nvfp4.FAST_MATH, offs, 2, 0, 0, 0, 0, ctypes.byref(out),
                None) == nvfp4.ERR_UNSUPPORTED
-    assert grp(ctypes.byref(_inp(16, 32, 32)), 1, offs, 18, 0, 0, 0, 0, ctypes.byref(out), None) == \
-        nvfp4.ERR_INVALID_ARG  # more groups than rows + 1
+    assert grp(ctypes.byref(_inp(16, 32, 32)), 1, offs, 1 << 31, 0, 0, 0, 0, ctypes.byref(out), None) == \
+        nvfp4.ERR_INVALID_ARG  # 2^31 groups
     assert grp(ctypes.byref(_inp(16, 32, 32)), 1, None, 2, 0, 0, 0, 0, ctypes.byref(out), None) == \
         nvfp4.ERR_INVALID_ARG  # no offsets
     dq = lib.nvfp4_dequantize

@@ -684,13 +684,18 @@ def test_grouped_rows_each_with_its_own_scale(mode, swizzled):
 
 
 GROUP_CASES = {
-    # rows, cols, dtype, group offsets, mode, strided
+    # rows, cols, dtype, group offsets, mode, strided, amax given, NaN at (row, col)
     "fibonacci_groups": (520, 272, torch.bfloat16, [0, 1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 520],
-                         "rht_sr", False),
-    "one_row_groups": (200, 128, torch.bfloat16, list(range(201)), "sr", False),
-    "fp32_strided": (300, 240, torch.float32, [0, 129, 129, 130, 300], "4o6", True),
-    "tile_aligned": (512, 512, torch.bfloat16, [0, 128, 256, 256, 512], "rne", False),
-    "long_rows": (40, 53248, torch.bfloat16, [0, 7, 7, 40], "rht_sr", False),
+                         "rht_sr", False, False, None),
+    "one_row_groups": (200, 128, torch.bfloat16, list(range(201)), "sr", False, False, None),
+    "fp32_strided": (300, 240, torch.float32, [0, 129, 129, 130, 300], "4o6", True, False, None),
+    "tile_aligned": (512, 512, torch.bfloat16, [0, 128, 256, 256, 512], "rne", False, False, None),
+    "long_rows": (40, 53248, torch.bfloat16, [0, 7, 7, 40], "rht_sr", False, False, None),
+    "empty_ends_given_fp32": (260, 96, torch.float32, [0, 0, 0, 130, 130, 260, 260], "sr", False, True, None),
+    "nan_in_one_group": (384, 160, torch.bfloat16, [0, 100, 250, 384], "rht_sr", False, False, (120, 37)),
+    # 64 experts, 10 tokens: most groups empty
+    "more_groups_than_rows": (10, 64, torch.bfloat16, [0] * 20 + [3] * 20 + [7] * 10 + [10] * 15, "rht_sr", False,
+                              False, None),
 }
 
 
@@ -700,9 +705,11 @@ def test_grouped_tiles(case):
     one tile (their rows look divisors up without a table), a group per row,
     fp32 rows with a pitch, boundaries on tile edges, and rows longer than
     96 KiB; ragged column tiles and pad rows in the swizzled layout."""
-    R, C, dtype, offs, mode, strided = GROUP_CASES[case]
+    R, C, dtype, offs, mode, strided, given, nan_at = GROUP_CASES[case]
     x = mixed_input(R, C, seed=31 + list(GROUP_CASES).index(case), dtype=dtype)
     x[offs[1]:offs[2]] *= 1e-2  # a group with a scale of its own
+    if nan_at:
+        x[nan_at] = float("nan")  # poisons its group's amax and scale, no other group
     if strided:
         base = torch.zeros(R, C + 32, dtype=dtype, device="cuda")
         base[:, 16:16 + C] = x.cuda()
@@ -711,13 +718,32 @@ def test_grouped_tiles(case):
         x_dev = to_device(x)
     kw = dict(mode=mode, swizzled=True, sign_mask=0x1DB7, seed=15, offset=6)
     offs_d = torch.tensor(offs, dtype=torch.int64, device="cuda")
-    q = nvfp4.quantize_grouped(x_dev, offs_d, **kw)
+    A = None
+    if given:  # twice each group's own amax (an empty group's stays 0)
+        A = _oracle_grouped(x, offs, **kw)[2] * np.float32(2.0)
+    q = nvfp4.quantize_grouped(x_dev, offs_d, amax=None if A is None else torch.from_numpy(A).cuda(), **kw)
     torch.cuda.synchronize()
-    codes, scales, amaxes, gscales = _oracle_grouped(x, offs, **kw)
+    codes, scales, amaxes, gscales = _oracle_grouped(x, offs, amax=A, **kw)
+    if nan_at:
+        assert np.isnan(amaxes[1]) and not np.isnan(np.delete(amaxes, 1)).any()
     assert np.array_equal(q.codes_row.cpu().numpy(), codes)
     assert np.array_equal(q.scales_row.cpu().numpy(), scales)
     assert same_float_bits(q.amax.cpu().numpy(), amaxes)
     assert same_float_bits(q.global_scale.cpu().numpy(), gscales)
+
+
+def test_grouped_empty_input():
+    """No rows: every group is empty, its amax and scale 0 (given amaxes kept)."""
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    offs_d = torch.zeros(4, dtype=torch.int64, device="cuda")
+    q = nvfp4.quantize_grouped(x, offs_d, mode="rht_sr", sign_mask=0x1234, seed=1)
+    torch.cuda.synchronize()
+    assert q.amax.cpu().tolist() == [0.0, 0.0, 0.0] and q.global_scale.cpu().tolist() == [0.0, 0.0, 0.0]
+    A = torch.tensor([2688.0, 0.0, 5376.0], device="cuda")
+    q = nvfp4.quantize_grouped(x, offs_d, mode="sr", amax=A)
+    torch.cuda.synchronize()
+    assert q.amax.cpu().tolist() == [2688.0, 0.0, 5376.0]
+    assert q.global_scale.cpu().tolist() == [1.0, 0.0, 2.0]
 
 
 def test_grouped_one_group_is_the_per_tensor_result():
