@@ -220,8 +220,8 @@ __global__ void __launch_bounds__(16 * kColRBT) k_quant_col(const __grid_constan
             const uint32_t t = blockIdx.x + k * gridDim.x;
             if (t < ntiles) {
                 mbar_arrive_expect_tx(&full[k], CT::kStageBytes);
-                tma_load_2d(in + k * CT::kStageBytes, &tmap, (int32_t)((t % ntc) * TC),
-                            (int32_t)((t / ntc) * CT::TR), &full[k]);
+                tma_load_2d(in + k * CT::kStageBytes, &tmap, (int32_t)(((ntiles - 1 - t) % ntc) * TC),
+                            (int32_t)(((ntiles - 1 - t) / ntc) * CT::TR), &full[k]);
             }
         }
     }
@@ -244,7 +244,9 @@ __global__ void __launch_bounds__(16 * kColRBT) k_quant_col(const __grid_constan
         if (!mbar_wait(&full[s], (k >> 1) & 1u)) {
             wait_gave_up(a, a.gscale);
         }
-        const uint32_t tr = t / ntc, tc = t - tr * ntc;
+        // tiles from the end of the tensor: the amax pass read the tail last, so
+        // with a tensor larger than L2 the first tiles here still come from L2
+        const uint32_t tr = (ntiles - 1 - t) / ntc, tc = (ntiles - 1 - t) - tr * ntc;
         const uint32_t rb = tr * RBT + rbl, o0 = tc * TC;
         const uint8_t *stage = in + s * CT::kStageBytes;
 #pragma unroll
@@ -290,8 +292,8 @@ __global__ void __launch_bounds__(16 * kColRBT) k_quant_col(const __grid_constan
             if (tn < ntiles) {
                 fence_async_shared();
                 mbar_arrive_expect_tx(&full[s], CT::kStageBytes);
-                tma_load_2d(in + s * CT::kStageBytes, &tmap, (int32_t)((tn % ntc) * TC),
-                            (int32_t)((tn / ntc) * CT::TR), &full[s]);
+                tma_load_2d(in + s * CT::kStageBytes, &tmap, (int32_t)(((ntiles - 1 - tn) % ntc) * TC),
+                            (int32_t)(((ntiles - 1 - tn) / ntc) * CT::TR), &full[s]);
             }
         }
     }
@@ -338,8 +340,8 @@ __global__ void __launch_bounds__(16 * kColRBT, 5) k_quant_2d(const __grid_const
             const uint32_t t = blockIdx.x + k * gridDim.x;
             if (t < ntiles) {
                 mbar_arrive_expect_tx(&full[k], CT::kStageBytes);
-                tma_load_2d(in + k * CT::kStageBytes, &tmap, (int32_t)((t % ntc) * TC),
-                            (int32_t)((t / ntc) * CT::TR), &full[k]);
+                tma_load_2d(in + k * CT::kStageBytes, &tmap, (int32_t)(((ntiles - 1 - t) % ntc) * TC),
+                            (int32_t)(((ntiles - 1 - t) / ntc) * CT::TR), &full[k]);
             }
         }
     }
@@ -366,7 +368,9 @@ __global__ void __launch_bounds__(16 * kColRBT, 5) k_quant_2d(const __grid_const
         if (!mbar_wait(&full[s], (k >> 1) & 1u)) {
             wait_gave_up(a, a.gscale);
         }
-        const uint32_t tr = t / ntc, tc = t - tr * ntc;
+        // tiles from the end of the tensor: the amax pass read the tail last, so
+        // with a tensor larger than L2 the first tiles here still come from L2
+        const uint32_t tr = (ntiles - 1 - t) / ntc, tc = (ntiles - 1 - t) - tr * ntc;
         const uint32_t rb0 = tr * RBT, o0 = tc * TC, rb = rb0 + rbl, ob = o0 + HC * hc;
         const bool valid = rb < RB && ob < C;  // C % 16 == 0: a 16x16 tile is all in or all out
         const uint8_t *stage = in + s * CT::kStageBytes;
@@ -489,8 +493,8 @@ __global__ void __launch_bounds__(16 * kColRBT, 5) k_quant_2d(const __grid_const
             if (tn < ntiles) {
                 fence_async_shared();
                 mbar_arrive_expect_tx(&full[s], CT::kStageBytes);
-                tma_load_2d(in + s * CT::kStageBytes, &tmap, (int32_t)((tn % ntc) * TC),
-                            (int32_t)((tn / ntc) * CT::TR), &full[s]);
+                tma_load_2d(in + s * CT::kStageBytes, &tmap, (int32_t)(((ntiles - 1 - tn) % ntc) * TC),
+                            (int32_t)(((ntiles - 1 - tn) / ntc) * CT::TR), &full[s]);
             }
         }
         if (a.want_col)

@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
     }
     for (int k = 0; k < kStages; k++) {
         if (tid == 0 && blockIdx.x + k * G < ntiles)
-            issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], ir, ic);
+            issue_tile<T>(&tmap, stages + k * RowTile<T>::kStageBytes, &full[k], ntr - 1 - ir, ntc - 1 - ic);
         advance(ir, ic);
     }
     // per-scale state, built while the first copies are in flight; the amax
@@ -277,7 +277,10 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
         if (!mbar_wait(&full[s], (k / kStages) & 1u)) {  // a copy never landed: bounded, visible failure
             wait_gave_up(a, a.gscale);
         }
-        const uint32_t row = tr * kTileRows + tid, j0 = tc * 4;
+        // tiles from the end of the tensor: the amax pass read the tail last, so
+        // with a tensor larger than L2 the first tiles here still come from L2
+        // (-0.9 us at 16384x8192; no change when the whole input fits)
+        const uint32_t row = (ntr - 1 - tr) * kTileRows + tid, j0 = (ntc - 1 - tc) * 4;
         const uint8_t *stage = stages + s * RowTile<T>::kStageBytes;
         if (row < R) {
             encode_tile_row<MODE, RHT, T, AP>(a, stage, tid, row, j0, C, CS, csp, tab, sd, rm, signs, fast, codes16,
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kTileRows) k_quant_row(const __grid_constant__
         __syncthreads();  // every thread is done with stage s
         if (tid == 0 && t + kStages * G < ntiles) {
             fence_async_shared();
-            issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], ir, ic);
+            issue_tile<T>(&tmap, stages + s * RowTile<T>::kStageBytes, &full[s], ntr - 1 - ir, ntc - 1 - ic);
         }
         advance(ir, ic);
     }
