@@ -47,7 +47,7 @@ def _lib():
         lib = ctypes.CDLL(build())
         i64, i32, u32, u64, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
         lib.ora_quantize.argtypes = [vp, i32, i64, i64, i64, i32, i32, i32, i32, i32, i32, u32,
-                                     u64, u64, i64, i64, vp, vp, vp, vp, vp]
+                                     u64, u64, i64, i64, vp, vp, vp, vp, vp, u64]
         lib.ora_quantize.restype = i32
         lib.ora_dequantize.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, i32]
         lib.ora_dequantize.restype = i32
@@ -115,12 +115,14 @@ def scale_bytes(rows_out: int, cols_out: int, swizzled: bool) -> int:
 def quantize(x: np.ndarray, *, colwise: bool = False, mode: str = "rne", block2d: bool = False,
              per_row: bool = False, swizzled: bool = False, rht: bool = False, sign_mask: int = 0,
              seed: int = 0, offset: int = 0, row_range: tuple[int, int] | None = None,
-             amax_given: float | None = None) -> dict:
+             amax_given: float | None = None, block_base: int = 0) -> dict:
     """Quantize one orientation of ``x``; returns codes, scales, amax, global_scale.
 
     ``colwise`` works on X^T.  ``row_range`` restricts encoding to output rows
     [r0, r1) (the per-tensor amax still covers the whole tensor); rows outside
     the range are left zero.  ``amax_given`` replaces the per-tensor amax.
+    ``block_base`` is added to every block number of the Philox counter: the
+    number of this input's first block when it is a shard of a larger tensor.
     """
     x, dtype, ld = _input(x)
     rows, cols = x.shape
@@ -135,7 +137,7 @@ def quantize(x: np.ndarray, *, colwise: bool = False, mode: str = "rne", block2d
     rc = _lib().ora_quantize(_ptr(x), dtype, rows, cols, ld, int(colwise), MODES[mode], int(block2d),
                              int(per_row), int(swizzled), int(rht), sign_mask & 0xFFFF, seed, offset,
                              r0, r1, None if given is None else _ptr(given),
-                             _ptr(codes), _ptr(scales), _ptr(amax), _ptr(gs))
+                             _ptr(codes), _ptr(scales), _ptr(amax), _ptr(gs), block_base)
     if rc != 0:
         raise ValueError(f"oracle quantize rejected the arguments (status {rc})")
     if not swizzled:
@@ -208,7 +210,7 @@ def quantize_parallel(x: np.ndarray, *, threads: int | None = None, colwise: boo
         rc = lib.ora_quantize(_ptr(x), dtype, rows, cols, ld, int(colwise), MODES[mode], int(block2d),
                               int(per_row), int(swizzled), int(rht), sign_mask & 0xFFFF, seed, offset,
                               r0, r1, None if given is None else _ptr(given),
-                              _ptr(codes), _ptr(scales), _ptr(a), _ptr(g))
+                              _ptr(codes), _ptr(scales), _ptr(a), _ptr(g), 0)
         return rc, a, g
 
     with ThreadPoolExecutor(n) as ex:

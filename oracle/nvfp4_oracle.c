@@ -302,12 +302,15 @@ static void load_block(const view_t *v, int64_t r, int64_t j, int rht, uint32_t 
  *            over the WHOLE tensor whatever [r0, r1) is).
  * codes: [R_out, C_out/2] bytes, low nibble = even element.  scales: linear
  * [R_out, C_out/16] or swizzled.  amax_out / gscale_out: 1 float (per tensor)
- * or R_out floats (per row; only [r0, r1) written). */
+ * or R_out floats (per row; only [r0, r1) written).
+ *   block_base: added to every block number of the Philox counter, i.e. the
+ *            number of this input's first block when it is a shard of a larger
+ *            tensor whose blocks keep their numbers (0 for a whole tensor). */
 int ora_quantize(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                  int orient, int mode, int block2d, int per_row, int swizzled,
                  int rht, uint32_t sign_mask, uint64_t seed, uint64_t offset,
                  int64_t r0, int64_t r1, const float *amax_in,
-                 uint8_t *codes, uint8_t *scales, float *amax_out, float *gscale_out) {
+                 uint8_t *codes, uint8_t *scales, float *amax_out, float *gscale_out, uint64_t block_base) {
     view_t v = {x, dtype, rows, cols, ld, orient};
     int64_t R = orient ? cols : rows, C = orient ? rows : cols;
     if (!x || !codes || !scales || !amax_out || !gscale_out) return ORA_ERR_ARG;
@@ -391,7 +394,7 @@ int ora_quantize(const void *x, int dtype, int64_t rows, int64_t cols, int64_t l
                 memcpy(code, pick4 ? c4 : c6, sizeof code);
             } else {
                 uint8_t rb[16];
-                if (mode == ORA_MODE_SR) block_random_bytes(seed, offset, (uint64_t)(r * CS + j), rb);
+                if (mode == ORA_MODE_SR) block_random_bytes(seed, offset, block_base + (uint64_t)(r * CS + j), rb);
                 S = block_scale(amax_b, 6.0f, g);
                 encode_with_scale(y, 16, S, g, mode == ORA_MODE_SR, rb, code);
             }

@@ -44,6 +44,17 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t elem_size(int32_t dtype) { return dtype == NVFP4_IN_FP32 ? 4 : 2; }
 
+// Philox4x32-10 round keys of a seed: key + round * Weyl constant, on the
+// host once per call so that kernels read them from the parameter bank.
+void set_philox(nvfp4::QArgs &a, uint64_t seed, uint64_t offset) {
+    a.seed = seed;
+    a.offset = offset;
+    for (int i = 0; i < 10; i++) {
+        a.round_key0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
+        a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+    }
+}
+
 // Shape, stride and pointer checks shared by every entry point that reads X.
 nvfp4_status check_input(const nvfp4_input *in) {
     if (!in) return NVFP4_ERR_INVALID_ARG;
@@ -124,10 +135,7 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
     a.sign_mask = sign_mask;
     a.seed = seed;
     a.offset = offset;
-    for (int i = 0; i < 10; i++) {
-        a.round_key0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
-        a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
-    }
+    set_philox(a, seed, offset);
     a.fast_math = (flags & NVFP4_FAST_MATH) ? 1 : 0;
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
     const uint64_t base_row = (uint64_t)in->row0 * (uint64_t)(in->cols / 16);  // rowwise block numbers
@@ -279,10 +287,7 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
     a.sign_mask = sign_mask;
     a.seed = seed;
     a.offset = offset;
-    for (int i = 0; i < 10; i++) {
-        a.round_key0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
-        a.round_key1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
-    }
+    set_philox(a, seed, offset);
     a.blk_base = (uint64_t)in->row0 * (uint64_t)(in->cols / 16);
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
     const int kmode = mode == NVFP4_MODE_RNE ? nvfp4::MODE_RNE_ID

@@ -525,6 +525,27 @@ def test_row_shards_reproduce_the_whole_tensor():
         assert same_float_bits(part["global_scale"], whole["global_scale"])
 
 
+@pytest.mark.parametrize("given", [True, False], ids=["amax_given", "one_kernel"])
+@pytest.mark.parametrize("mode", ["sr", "rht_sr"])
+@pytest.mark.parametrize("row0", [2 ** 27 + 3, 2 ** 26 - 2], ids=["above_2e32", "across_2e32"])
+def test_block_counters_with_a_high_word(row0, mode, given):
+    """A row shard far into a tensor: its Philox block counters (row0 * C/16
+    onward) have their high word set, or cross 2^32 inside the call, with a
+    64-bit seed and offset.  The oracle numbers the same blocks (block_base)."""
+    R, C = 256, 1024
+    x = mixed_input(R, C, seed=41 + (row0 & 7))
+    xb = np_bits(x)
+    rht = mode == "rht_sr"
+    kw = dict(mode="sr", rht=rht, sign_mask=0x2D4B, seed=0x9E37_79B9_7F4A_7C15, offset=0xD1B5_4A32_D192_ED03,
+              swizzled=True)
+    A = oracle.amax(xb, rht=rht, sign_mask=kw["sign_mask"])[0]
+    want = oracle.quantize(xb, amax_given=float(A[0]) if given else None, block_base=row0 * (C // 16), **kw)
+    got = gpu_run(x, amax=torch.from_numpy(A).cuda() if given else None, row0=row0, **kw)
+    assert np.array_equal(got["codes_row"], want["codes"])
+    assert np.array_equal(got["scales_row"], want["scales"].ravel())
+    assert same_float_bits(got["global_scale"], want["global_scale"])
+
+
 @pytest.mark.parametrize("rht", [False, True])
 def test_column_shards_reproduce_the_whole_tensor(rht):
     x = mixed_input(256, 1024, seed=22)
@@ -693,6 +714,7 @@ GROUP_CASES = {
     "long_rows": (40, 53248, torch.bfloat16, [0, 7, 7, 40], "rht_sr", False, False, None),
     "empty_ends_given_fp32": (260, 96, torch.float32, [0, 0, 0, 130, 130, 260, 260], "sr", False, True, None),
     "nan_in_one_group": (384, 160, torch.bfloat16, [0, 100, 250, 384], "rht_sr", False, False, (120, 37)),
+    "fp32_rht": (200, 128, torch.float32, [0, 60, 61, 200], "rht_sr", False, False, None),
     # 64 experts, 10 tokens: most groups empty
     "more_groups_than_rows": (10, 64, torch.bfloat16, [0] * 20 + [3] * 20 + [7] * 10 + [10] * 15, "rht_sr", False,
                               False, None),

@@ -270,6 +270,33 @@ def test_sr_counter_layout(torch_philox):
             assert nib == (3 if byte >= 128 else 2), (r, j, e, byte, nib)
 
 
+@pytest.mark.parametrize("base", [16, 2 ** 32 - 6, 2 ** 33 + 5, 2 ** 62])
+def test_sr_counter_block_base(torch_philox, base):
+    """A shard whose blocks keep their numbers in the whole tensor: block (r, j)
+    draws counter (base + r * (C/16) + j, offset), also across and above 2^32
+    (the counter's high word), with a 64-bit seed and offset.  Same half-way
+    construction as above: the codes expose the top bit of every random byte."""
+    R, C = 3, 64
+    x = np.zeros((R, C), np.float32)
+    for j in range(C // 16):
+        x[:, 16 * j] = 6.0
+        x[:, 16 * j + 1:16 * j + 16] = 1.25
+    seed, offset = 0x9E37_79B9_7F4A_7C15, 0xD1B5_4A32_D192_ED03
+    codes = oracle.quantize(x, mode="sr", seed=seed, offset=offset, block_base=base)["codes"]
+    blks = [(r, j) for r in range(R) for j in range(C // 16)]
+    ref = torch_philox([(seed, offset, base + r * (C // 16) + j) for r, j in blks])
+    for (r, j), words in zip(blks, ref):
+        for e in range(1, 16):
+            byte = (words[e >> 2] >> (8 * (e & 3))) & 0xFF
+            nib = (codes[r, 8 * j + e // 2] >> (4 * (e & 1))) & 15
+            assert nib == (3 if byte >= 128 else 2), (base, r, j, e)
+    # and base 0 with the rows of a taller tensor is the row range of that tensor
+    tall = np.concatenate([x, x, x])
+    whole = oracle.quantize(tall, mode="sr", seed=seed, offset=offset, row_range=(R, 2 * R), amax_given=6.0)
+    part = oracle.quantize(x, mode="sr", seed=seed, offset=offset, amax_given=6.0, block_base=R * (C // 16))
+    assert np.array_equal(whole["codes"][R:2 * R], part["codes"])
+
+
 # ----------------------------------------------------------------- RHT
 def hadamard16():
     return [[(-1) ** bin(i & j).count("1") for j in range(16)] for i in range(16)]
