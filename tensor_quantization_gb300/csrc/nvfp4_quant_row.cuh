@@ -7,6 +7,10 @@
 //                            or given by the caller).  TMA brings 128-row
 //                            tiles into shared memory; a thread encodes the
 //                            four blocks of one tile row.
+//  k_quant_row_grouped       the same tiles for row groups, each row encoded
+//                            with its group's global scale.
+//  k_quant_row_fused         small per-tensor inputs: amax pass, grid barrier
+//                            and encode in one cooperative launch.
 //  k_quant_rowscaled_staged  one global scale per row, rows of up to 96 KiB:
 //                            a CTA stages whole rows in shared memory with
 //                            bulk copies, reduces each row's amax, prepares
