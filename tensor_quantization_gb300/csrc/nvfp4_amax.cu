@@ -428,12 +428,17 @@ __global__ void __launch_bounds__(256) k_amax_rows(const QArgs a) {
 // s0 + i / CS, column i % CS: each thread keeps a (row, column) cursor that
 // advances by the CTA's thread count without a division, and has kLdgBlocks
 // blocks in flight.  With the RHT, a block whose butterfly bound is not above
-// the warp's running maximum of the segment skips the butterfly (the skip
-// test of k_amax_ldg_rht; the maximum restarts at 0 for every segment).
+// the CTA's running maximum of the segment skips the butterfly (the skip test
+// of k_amax_ldg_rht): each warp folds its maximum into a shared word once per
+// round and takes the word back as its threshold; the word restarts at 0 for
+// every segment, so it only ever holds maxima of the segment's own group.
+// (Sharing it through amax[g] across CTAs measured 2 us slower: every CTA of
+// a group updates the same word.)
 template <bool RHT, typename T>
 __global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_groups(const QArgs a) {
     constexpr bool SKIP = RHT && kAmaxSkip;
     __shared__ uint32_t red[32];
+    __shared__ uint32_t seg_max;
     const uint32_t CS = (uint32_t)(a.cols >> 4);
     const T *x = static_cast<const T *>(a.x);
     const int64_t per = (a.rows + gridDim.x - 1) / gridDim.x;
@@ -464,6 +469,10 @@ __global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_groups(const QArgs a) 
                 p -= back;  // one row down, CS blocks back
             }
         };
+        if (SKIP) {
+            if (threadIdx.x == 0) seg_max = 0u;
+            __syncthreads();
+        }
         uint32_t m = 0;
         auto reduce = [&](const RawBlock<T> &raw) {
             if (!RHT) {
@@ -486,7 +495,11 @@ __global__ void __launch_bounds__(kAmaxLdgThreads) k_amax_groups(const QArgs a) 
             }
 #pragma unroll
             for (int u = 0; u < kLdgBlocks; u++) reduce(raw[u]);
-            if (SKIP) m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (SKIP) {
+                m = __reduce_max_sync(0xFFFFFFFFu, m);
+                if (lane == 0) atomicMax(&seg_max, m);
+                m = max(m, *reinterpret_cast<volatile uint32_t *>(&seg_max));
+            }
         }
         for (; i < nb; i += nt) {
             RawBlock<T> raw;
