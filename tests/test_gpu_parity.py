@@ -715,6 +715,7 @@ GROUP_CASES = {
     "empty_ends_given_fp32": (260, 96, torch.float32, [0, 0, 0, 130, 130, 260, 260], "sr", False, True, None),
     "nan_in_one_group": (384, 160, torch.bfloat16, [0, 100, 250, 384], "rht_sr", False, False, (120, 37)),
     "fp32_rht": (200, 128, torch.float32, [0, 60, 61, 200], "rht_sr", False, False, None),
+    "zero_group": (200, 96, torch.bfloat16, [0, 64, 128, 200], "sr", False, False, None),
     # 64 experts, 10 tokens: most groups empty
     "more_groups_than_rows": (10, 64, torch.bfloat16, [0] * 20 + [3] * 20 + [7] * 10 + [10] * 15, "rht_sr", False,
                               False, None),
@@ -729,7 +730,7 @@ def test_grouped_tiles(case):
     96 KiB; ragged column tiles and pad rows in the swizzled layout."""
     R, C, dtype, offs, mode, strided, given, nan_at = GROUP_CASES[case]
     x = mixed_input(R, C, seed=31 + list(GROUP_CASES).index(case), dtype=dtype)
-    x[offs[1]:offs[2]] *= 1e-2  # a group with a scale of its own
+    x[offs[1]:offs[2]] *= 0.0 if case == "zero_group" else 1e-2  # a group with a scale of its own
     if nan_at:
         x[nan_at] = float("nan")  # poisons its group's amax and scale, no other group
     if strided:
