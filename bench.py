@@ -121,6 +121,18 @@ def profile_field(kernel: str, workload: str, field: str) -> float | None:
     return float(m.group(1))
 
 
+def choose_roofline(w: wl.Workload, hbm_view: dict, issue_view: dict | None, traffic) -> dict:
+    """The roofline a workload is judged against: plain ALU issue for the
+    per-row four-over-six path (two candidates per block), with its HBM view
+    beside it; HBM bandwidth of the counted bytes for the codec workloads, with
+    the issue rate the kernel runs at beside it (when ncu's count is known)."""
+    if issue_view is None:
+        return hbm_view
+    if w.per_row:
+        return dict(issue_view, traffic=traffic, hbm_view={k: hbm_view[k] for k in ("achieved", "peak", "unit", "frac")})
+    return dict(hbm_view, issue_view={k: issue_view[k] for k in ("achieved", "peak", "unit", "frac", "peak_source")})
+
+
 def profile_traffic(kernel: str, workload: str) -> float | None:
     return profile_field(kernel, workload, "traffic_bytes_per_launch")
 
@@ -397,16 +409,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
                       "instructions_per_launch": round(inst),
                       "instructions_source": f"ncu smsp__inst_executed.sum per element, profiles/{dom}__{w.name}.md",
                       "ms_per_launch": round(dom_ms, 5)}
-        if w.per_row:
-            # the per-row four-over-six path: plain ALU issue binds (two
-            # candidates per block); its HBM view rides along
-            roofline = dict(issue_view, traffic=traffic,
-                            hbm_view={k: hbm_view[k] for k in ("achieved", "peak", "unit", "frac")})
-        else:
-            # codec work: the HBM roofline of the counted bytes, with the issue
-            # rate the kernel actually runs at beside it
-            roofline = dict(hbm_view, issue_view={k: issue_view[k] for k in
-                                                  ("achieved", "peak", "unit", "frac", "peak_source")})
+        roofline = choose_roofline(w, hbm_view, issue_view, traffic)
     med = statistics.median(step_ms)
     cfg = bench_config(w, world)
     cfg["input_sha256"] = hashlib.sha256(x_cpu.contiguous().view(torch.int16).numpy().tobytes()).hexdigest()

@@ -54,3 +54,19 @@ def test_every_workload_is_planned():
     for w in wl.WORKLOADS.values():
         assert bench.call_kernels(w)
         assert bench.counted_bytes(w)["total"] > w.rows * w.cols * 2
+
+
+def test_roofline_choice_follows_the_measurement_plan():
+    """HBM for the codec workloads (issue rate beside it), ALU issue for the
+    per-row four-over-six workload (HBM beside it); HBM alone without ncu's
+    instruction count."""
+    hbm = {"bound": "hbm", "achieved": 3000.0, "peak": 6690.5, "unit": "GB/s", "frac": 0.448, "traffic": 7e6}
+    issue = {"bound": "alu", "achieved": 600.0, "peak": 1258.6, "unit": "Gwarp-inst/s", "frac": 0.477,
+             "peak_source": "x"}
+    for name, w in wl.WORKLOADS.items():
+        r = bench.choose_roofline(w, hbm, issue, 7e6)
+        if w.per_row:
+            assert r["bound"] == "alu" and r["hbm_view"]["frac"] == 0.448 and r["traffic"] == 7e6, name
+        else:
+            assert r["bound"] == "hbm" and r["issue_view"]["frac"] == 0.477 and r["traffic"] == 7e6, name
+        assert bench.choose_roofline(w, hbm, None, None) is hbm
