@@ -44,8 +44,9 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t elem_size(int32_t dtype) { return dtype == NVFP4_IN_FP32 ? 4 : 2; }
 
-// Philox4x32-10 round keys of a seed: key + round * Weyl constant, on the
-// host once per call so that kernels read them from the parameter bank.
+// The call's Philox4x32-10 seed and offset, and the round keys of the seed
+// (key + round * Weyl constant), computed on the host once per call so that
+// kernels read them from the parameter bank.
 void set_philox(nvfp4::QArgs &a, uint64_t seed, uint64_t offset) {
     a.seed = seed;
     a.offset = offset;
@@ -133,8 +134,6 @@ nvfp4_status quantize(const nvfp4_input *in, uint32_t flags, int mode, bool rht,
 
     nvfp4::QArgs a = make_args(in, out, ws, flags);
     a.sign_mask = sign_mask;
-    a.seed = seed;
-    a.offset = offset;
     set_philox(a, seed, offset);
     a.fast_math = (flags & NVFP4_FAST_MATH) ? 1 : 0;
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
@@ -285,8 +284,6 @@ nvfp4_status nvfp4_quantize_grouped(const nvfp4_input *in, uint32_t flags, const
     if (!out->codes_row || !out->scales_row || !aligned(out->codes_row, 8)) return NVFP4_ERR_INVALID_ARG;
 
     a.sign_mask = sign_mask;
-    a.seed = seed;
-    a.offset = offset;
     set_philox(a, seed, offset);
     a.blk_base = (uint64_t)in->row0 * (uint64_t)(in->cols / 16);
     const bool fp32 = in->dtype == NVFP4_IN_FP32;
